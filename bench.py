@@ -1,0 +1,570 @@
+#!/usr/bin/env python3
+"""Benchmark of the fused FSDP FlatParameter shard step on GB300.
+
+Default workload: one rank's step of the Llama-7B-shaped model (32 blocks of
+202,383,360 params + a root unit of 262,148,096; W = 8 virtual ranks,
+local-rank mode). One step = one fsdp_shard_step_grouped call over all 33
+units: reduce-scatter of the rank's slice of the 8 bf16 gradients, Adam on the
+rank's fp32 master/m/v shard, bf16 cast, and all-gather of the 7 other ranks'
+bf16 shards into the 33 full bf16 FlatParameters. Algorithmic bytes per shard
+element: 2W (gradients) + 24 (state read+write) + 2 (own bf16) + 4(W-1)
+(other shards read + written) = 70 at W = 8.
+
+Prints one JSON line (rank 0). Options pick other workloads for measurement
+notes; the default is the headline.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+                  [--impl ours|reference] [--no-e2e] [--no-cpu-baseline]
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "fused FSDP shard-step HBM GB/s and params/s, % of GB300 HBM peak"
+UNIT = "GB/s"
+KERNEL_SOURCES = ["fully_sharded_gb300/csrc/segment_kernel.cuh", "fully_sharded_gb300/csrc/abi.cu"]
+TRAFFIC_PROFILE = os.path.join(ROOT, "profiles", "segment_kernel_llama7b_local_rank.md")
+
+
+# ------------------------------------------------------------------ helpers
+
+def env_rank():
+    return int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")), \
+        int(os.environ.get("LOCAL_RANK", "0"))
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    for p in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, p), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(workload):
+    """Per-launch DRAM bytes from the committed ncu summary, if it was taken on this kernel source."""
+    if not os.path.exists(TRAFFIC_PROFILE):
+        return None
+    text = open(TRAFFIC_PROFILE).read()
+    m_src = re.search(r"kernel_source_sha256_16:\s*([0-9a-f]{16})", text)
+    m_wl = re.search(r"workload:\s*(\S+)", text)
+    m_b = re.search(r"dram_bytes_per_full_launch:\s*([0-9.eE+]+)", text)
+    if not (m_src and m_b and m_wl) or m_src.group(1) != kernel_source_hash() or m_wl.group(1) != workload:
+        return None
+    return float(m_b.group(1))
+
+
+class ClockSampler:
+    """nvidia-smi samples during the timed region."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.proc = None
+        self.gpu = gpu_index
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (FileNotFoundError, OSError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        rows = [r.split(",") for r in out.strip().splitlines() if r.strip()]
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            r = [x.strip() for x in r]
+            try:
+                sm.append(float(r[0]))
+                mx.append(float(r[1]))
+            except (ValueError, IndexError):
+                continue
+            for name, val in zip(names, r[4:8]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# --------------------------------------------------------------- workloads
+
+def build_local_rank(wl, rank, torch, fs, synth, hp_step=1):
+    """Device buffers of one rank's step over all units (local-rank mode)."""
+    from synth import workloads as wls
+    W = wl.world_size
+    lays = [fs.fsdp_flatten_layout(wls.numels(u), W)[0] for u in wl.units]
+    S_tot = sum(l.shard_numel for l in lays)
+    pad_tot = sum(l.padded_numel for l in lays)
+    maxpad = max(l.padded_numel for l in lays)
+    dev = torch.device("cuda")
+    # gradient pool: 2 unit-sets of W rows (units alternate between them)
+    slots = min(2, len(lays))
+    pool = [torch.empty((W, maxpad), dtype=torch.int16, device=dev) for _ in range(slots)]
+    for s in range(slots):
+        for k in range(W):
+            synth.fill_(pool[s][k], wls.key_grad(wl, s, k, 0), wl.sigma_grad)
+    master = torch.empty(S_tot, device=dev)
+    exp_avg = torch.empty(S_tot, device=dev)
+    exp_avg_sq = torch.empty(S_tot, device=dev)
+    others = torch.empty((W, S_tot), dtype=torch.int16, device=dev)
+    full = torch.empty(pad_tot, dtype=torch.int16, device=dev)
+    units = []
+    so = po = 0
+    for u, lay in enumerate(lays):
+        S, padded, P = lay.shard_numel, lay.padded_numel, lay.numel
+        sl = slice(so, so + S)
+        synth.fill_(master[sl], wls.key_master(wl, u), wl.sigma_master, idx0=rank * S, n_valid=P)
+        for buf, key in ((exp_avg, wls.key_exp_avg(wl, u)), (exp_avg_sq, wls.key_exp_avg_sq(wl, u))):
+            if wl.sigma_state:
+                synth.fill_(buf[sl], key, wl.sigma_state, idx0=rank * S, absval=True, n_valid=P)
+            else:
+                buf[sl].zero_()
+        oth = [None] * W
+        for k in range(W):
+            if k != rank:
+                synth.fill_(others[k, sl], wls.key_shard(wl, u), wl.sigma_master, idx0=k * S, n_valid=P)
+                oth[k] = others[k, sl]
+        units.append(dict(layout=lay, grads=[pool[u % slots][k, :padded] for k in range(W)],
+                          master=[master[sl]], exp_avg=[exp_avg[sl]], exp_avg_sq=[exp_avg_sq[sl]],
+                          other_shards=oth, full_out=[full[po:po + padded]]))
+        so += S
+        po += padded
+    torch.cuda.synchronize()
+    bytes_per_step = (6 * W + 22) * S_tot
+    info = dict(units=len(lays), W=W, rank=rank, params=sum(l.numel for l in lays),
+                shard_elems=S_tot, bytes_per_step=bytes_per_step, elems_per_step=S_tot,
+                mode="local-rank")
+    bufs = dict(pool=pool, master=master, exp_avg=exp_avg, exp_avg_sq=exp_avg_sq, others=others,
+                full=full)
+    return units, info, bufs
+
+
+def build_all_ranks(wl, F, torch, fs, synth):
+    """Device buffers of the all-ranks step (every rank's state updated, every group gathered)."""
+    from synth import workloads as wls
+    W = wl.world_size
+    R = W // F
+    dev = torch.device("cuda")
+    units = []
+    keep = []
+    S_sum = pad_sum = 0
+    for u, shapes in enumerate(wl.units):
+        lay = fs.fsdp_flatten_layout(wls.numels(shapes), W, F)[0]
+        S, padded, P = lay.shard_numel, lay.padded_numel, lay.numel
+        grads = torch.empty((W, padded), dtype=torch.int16, device=dev)
+        for k in range(W):
+            synth.fill_(grads[k], wls.key_grad(wl, u, k, 0), wl.sigma_grad, n_valid=P)
+        st = [torch.empty((R, padded), device=dev) for _ in range(3)]
+        for g in range(R):
+            synth.fill_(st[0][g], wls.key_master(wl, u), wl.sigma_master, n_valid=P)
+            for j, key in ((1, wls.key_exp_avg(wl, u)), (2, wls.key_exp_avg_sq(wl, u))):
+                if wl.sigma_state:
+                    synth.fill_(st[j][g], key, wl.sigma_state, absval=True, n_valid=P)
+                else:
+                    st[j][g].zero_()
+        full = torch.empty((R, padded), dtype=torch.int16, device=dev)
+        ranks = range(W)
+        units.append(dict(layout=lay, grads=[grads[k] for k in range(W)],
+                          master=[st[0][r // F, (r % F) * S:(r % F + 1) * S] for r in ranks],
+                          exp_avg=[st[1][r // F, (r % F) * S:(r % F + 1) * S] for r in ranks],
+                          exp_avg_sq=[st[2][r // F, (r % F) * S:(r % F + 1) * S] for r in ranks],
+                          other_shards=None, full_out=[full[g] for g in range(R)]))
+        keep.append((grads, st, full))
+        S_sum += S
+        pad_sum += padded
+    torch.cuda.synchronize()
+    # per padded element: W bf16 gradient reads, and per replica the fp32 master/m/v
+    # read + write (24) and the bf16 write into its group's full buffer (2)
+    bytes_per_step = (2 * W + 26 * R) * pad_sum
+    info = dict(units=len(wl.units), W=W, F=F, R=R, params=sum(u["layout"].numel for u in units),
+                padded_elems=pad_sum, bytes_per_step=bytes_per_step, elems_per_step=pad_sum,
+                mode="all-ranks")
+    return units, info, keep
+
+
+def build_sweep(n, W, torch, fs, synth):
+    from synth.workloads import Workload
+    wl = Workload("sweep", 6, [[(n,)]], W, sigma_state=1e-4)
+    return build_all_ranks(wl, W, torch, fs, synth)
+
+
+# ------------------------------------------------------------ the GPU arm
+
+def run_ours(args):
+    import torch
+    import fully_sharded_gb300 as fs
+    import synth
+    from synth import workloads as wls
+
+    rank, world, local_rank = env_rank()
+    torch.cuda.set_device(local_rank)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    name = args.workload
+    if name == "llama7b":
+        wl = wls.LLAMA7B
+        if args.units:
+            wl = wls.Workload(wl.name, wl.config_id, wl.units[:args.units], wl.world_size,
+                              sigma_state=wl.sigma_state)
+        vrank = rank % wl.world_size
+        units, info, bufs = build_local_rank(wl, vrank, torch, fs, synth)
+        rb, re = vrank, vrank + 1
+        workload_name = "llama7b_local_rank" + ("_units%d" % args.units if args.units else "")
+    elif name in ("llama_block", "gpt2_small"):
+        wl = wls.ALL[name]
+        units, info, bufs = build_all_ranks(wl, wl.world_size, torch, fs, synth)
+        rb, re = 0, wl.world_size
+        workload_name = name + "_all_ranks"
+    elif name.startswith("hybrid"):
+        F = int(name.split("_F")[1]) if "_F" in name else 16
+        wl = wls.HYBRID
+        units, info, bufs = build_all_ranks(wl, F, torch, fs, synth)
+        rb, re = 0, wl.world_size
+        workload_name = "hybrid_W16_F%d" % F
+    elif name.startswith("sweep"):
+        # sweep_<n>_W<w>
+        _, n, w = name.split("_")
+        units, info, bufs = build_sweep(int(float(n)), int(w[1:]), torch, fs, synth)
+        rb, re = 0, int(w[1:])
+        workload_name = name
+    else:
+        raise SystemExit("unknown workload %s" % name)
+    batch = fs.UnitBatch(units)
+    launches_per_step = fs.fsdp_shard_step_grouped_launches(batch, rb, re)
+    stream = torch.cuda.Stream()
+
+    # warm-up
+    t = 1
+    for _ in range(args.warmup):
+        fs.fsdp_shard_step_grouped(batch, rb, re, fs.AdamHyper(step=t), stream=stream)
+        t += 1
+    torch.cuda.synchronize()
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(args.steps)]
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    visible = os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",")
+    clocks = ClockSampler(visible[local_rank].strip() if len(visible) > local_rank and visible[local_rank].strip()
+                          else torch.cuda.current_device())
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.3)
+    stream.record_event(start)
+    for i in range(args.steps):
+        stream.record_event(evs[i][0])
+        fs.fsdp_shard_step_grouped(batch, rb, re, fs.AdamHyper(step=t), stream=stream)
+        stream.record_event(evs[i][1])
+        t += 1
+    stream.record_event(stop)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    if dist:
+        dist.barrier()
+    total_ms = start.elapsed_time(stop)
+    launch_ms = [a.elapsed_time(b) for a, b in evs]
+    if dist:
+        tt = torch.tensor([total_ms], device="cuda")
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        total_ms = float(tt.item())
+    ms_per_step = total_ms / args.steps
+    nproc = world
+    bytes_step = info["bytes_per_step"]
+    value = bytes_step * nproc / (ms_per_step * 1e-3) / 1e9
+    peak, peak_kind = measured_peaks()
+    mean_launch_ms = statistics.mean(launch_ms) / launches_per_step
+    achieved = bytes_step / launches_per_step / (mean_launch_ms * 1e-3) / 1e9
+    traffic = profiled_traffic(workload_name)
+    line = {
+        "metric": METRIC,
+        "value": round(value, 2),
+        "unit": UNIT,
+        "n_gpus": nproc,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_per_step, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f32",
+        "data": "synthetic",
+        "config": {
+            "workload": workload_name,
+            "W": info["W"],
+            "units": info["units"],
+            "params": info["params"],
+            "elems_per_step": info["elems_per_step"],
+            "algorithmic_bytes_per_step": bytes_step,
+            "mode": info["mode"],
+            "parallelism": "W=%d virtual ranks in one GPU's HBM; %d GPU process(es), each an independent "
+                           "step, no data-path collective" % (info["W"], nproc),
+            "l2": "inputs larger than L2: %.1f GB touched per step vs 129 MB L2" % (bytes_step / 1e9),
+            "storage": "bf16 gradients/params, fp32 master/m/v",
+        },
+        "params_per_s": round(info["elems_per_step"] * nproc / (ms_per_step * 1e-3), 1),
+        "pct_of_hbm_peak": round(100.0 * value / nproc / peak, 2),
+        "pct_of_nominal_8tbs": round(100.0 * value / nproc / 8000.0, 2),
+        "roofline": {
+            "bound": "hbm",
+            "achieved": round(achieved, 2),
+            "peak": peak,
+            "unit": "GB/s",
+            "frac": round(achieved / peak, 4),
+            "peak_source": peak_kind,
+            "kernel": "fsdp::segment_kernel<%d>" % (info["W"] if info["W"] in (1, 2, 4, 8, 16) else 0),
+            "traffic": traffic,
+        },
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clk,
+    }
+    if not args.no_e2e and name == "llama7b" and not args.units:
+        line["e2e"] = e2e_local_rank(args, torch, fs, synth, wls.LLAMA7B, units, info, bufs, rb, stream,
+                                     nproc, dist)
+    if rank == 0 and not args.no_cpu_baseline and name == "llama7b":
+        line["cpu_baseline"] = cpu_baseline(units, info, bufs, rb, torch, seconds=args.cpu_seconds)
+    if dist:
+        dist.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def e2e_local_rank(args, torch, fs, synth, wl, units, info, bufs, rank, stream, nproc, dist):
+    """Same metric through the public API with host buffers.
+
+    Per step: host->device copy (pinned memory) of the step's inputs, i.e. the
+    rank's slice of each of the W gradients of every unit, then the per-unit
+    fsdp_shard_step calls, then device->host read of the step's result, the
+    rank's updated bf16 shard of every unit. A second stream copies unit u+1's
+    gradients while unit u computes; the two-slot gradient pool bounds that
+    prefetch to one unit (the transient budget with prefetch = 1)."""
+    W = info["W"]
+    lays = [u["layout"] for u in units]
+    S_tot = info["shard_elems"]
+    # pinned host copies of the inputs each step consumes: W slices of S per unit
+    host_g = torch.empty((W, S_tot), dtype=torch.int16, pin_memory=True)
+    so = 0
+    for u, lay in enumerate(lays):
+        S = lay.shard_numel
+        for k in range(W):
+            host_g[k, so:so + S].copy_(units[u]["grads"][k][rank * S:(rank + 1) * S])
+        so += S
+    host_out = torch.empty(S_tot, dtype=torch.int16, pin_memory=True)
+    copy_stream = torch.cuda.Stream()
+    done = [torch.cuda.Event() for _ in range(2)]  # slot free again
+    ready = [torch.cuda.Event() for _ in range(len(lays))]
+    h2d_bytes = 2 * W * S_tot
+    d2h_bytes = 2 * S_tot
+
+    def one_step(t):
+        so = 0
+        offs = []
+        for u, lay in enumerate(lays):
+            offs.append(so)
+            so += lay.shard_numel
+        for u, lay in enumerate(lays):
+            S = lay.shard_numel
+            slot = u % 2
+            with torch.cuda.stream(copy_stream):
+                copy_stream.wait_event(done[slot])  # the unit that last used this slot is done
+                for k in range(W):
+                    units[u]["grads"][k][rank * S:(rank + 1) * S].copy_(
+                        host_g[k, offs[u]:offs[u] + S], non_blocking=True)
+                copy_stream.record_event(ready[u])
+            stream.wait_event(ready[u])
+            fs.fsdp_shard_step(units[u]["grads"], lay, rank, rank + 1, units[u]["master"],
+                               units[u]["exp_avg"], units[u]["exp_avg_sq"], units[u]["other_shards"],
+                               units[u]["full_out"], fs.AdamHyper(step=t), stream=stream)
+            stream.record_event(done[slot])
+            with torch.cuda.stream(stream):
+                host_out[offs[u]:offs[u] + S].copy_(
+                    units[u]["full_out"][0][rank * S:(rank + 1) * S], non_blocking=True)
+
+    t = 10_000
+    for _ in range(max(1, args.warmup)):
+        one_step(t)
+        t += 1
+    torch.cuda.synchronize()
+    k = max(1, min(args.steps, args.e2e_steps))
+    if dist:
+        dist.barrier()
+    t0 = time.perf_counter()
+    for _ in range(k):
+        one_step(t)
+        t += 1
+    torch.cuda.synchronize()
+    ms = (time.perf_counter() - t0) * 1e3 / k
+    if dist:
+        tt = torch.tensor([ms], device="cuda")
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        ms = float(tt.item())
+    return {"value": round(info["bytes_per_step"] * nproc / (ms * 1e-3) / 1e9, 2), "unit": UNIT,
+            "h2d_bytes_per_step": h2d_bytes, "d2h_bytes_per_step": d2h_bytes, "ms_per_step": round(ms, 3),
+            "steps": k, "note": "host wall clock around K steps, pinned buffers, per-unit calls"}
+
+
+# -------------------------------------------------------- CPU oracle (baseline)
+
+def oracle_sample_inputs(units, rank, n_s, torch):
+    """Unit 0 of the workload restricted to the first n_s elements of the rank's shard,
+    copied to the host: gradients' rank slices, state and the other ranks' shards."""
+    import numpy as np
+    u = units[0]
+    W = len(u["grads"])
+    S = u["layout"].shard_numel
+    n_s = min(n_s, S)
+    grads = np.zeros((W, W * n_s), dtype=np.uint16)
+    for k in range(W):
+        grads[k, rank * n_s:(rank + 1) * n_s] = (
+            u["grads"][k][rank * S:rank * S + n_s].cpu().numpy().view(np.uint16))
+    master = u["master"][0][:n_s].cpu().numpy().copy()
+    m = u["exp_avg"][0][:n_s].cpu().numpy().copy()
+    v = u["exp_avg_sq"][0][:n_s].cpu().numpy().copy()
+    others = [None if o is None else o[:n_s].cpu().numpy().view(np.uint16).copy()
+              for o in u["other_shards"]]
+    return grads, master, m, v, others, n_s
+
+
+def run_oracle_step(ora, grads, master, m, v, others, rank, n_s, step):
+    import numpy as np
+    W = grads.shape[0]
+    full = [np.zeros(W * n_s, np.uint16)]
+    ora.shard_step(list(grads), W, rank, rank + 1, [master], [m], [v], others, full,
+                   lr=1e-3, beta1=0.9, beta2=0.999, eps=1e-8, step=step)
+
+
+def cpu_baseline(units, info, bufs, rank, torch, seconds=10.0, n_s=1 << 22):
+    import oracle
+    ora = oracle.load()
+    grads, master, m, v, others, n_s = oracle_sample_inputs(units, rank, n_s, torch)
+    W = info["W"]
+    per = (6 * W + 22) * n_s
+    t0 = time.perf_counter()
+    reps = 0
+    while True:
+        run_oracle_step(ora, grads, master, m, v, others, rank, n_s, reps + 1)
+        reps += 1
+        if time.perf_counter() - t0 >= seconds:
+            break
+    dt = time.perf_counter() - t0
+    return {"value": round(per * reps / dt / 1e9, 4), "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": "unit 0 (one Llama block) of the workload, first %d elements of rank %d's "
+                      "shard (W=%d), %d repetitions in %.1f s; same algorithmic bytes per element"
+                      % (n_s, rank, W, reps, dt)}
+
+
+# ----------------------------------------------------------- reference arm
+
+def run_reference(args):
+    """The oracle timed on the host cores on a bounded sample of the same workload."""
+    rank, world, _ = env_rank()
+    if rank != 0:
+        return
+    import numpy as np
+    import oracle
+    import synth
+    from synth import workloads as wls
+    import fully_sharded_gb300 as fs
+    ora = oracle.load()
+    wl = wls.LLAMA7B
+    W = wl.world_size
+    lay = fs.fsdp_flatten_layout(wls.numels(wl.units[0]), W)[0]
+    S = lay.shard_numel
+    n_s = args.ref_sample
+    r = 0
+    grads = np.zeros((W, W * n_s), dtype=np.uint16)
+    for k in range(W):
+        grads[k, r * n_s:(r + 1) * n_s] = synth.normal_bf16(wls.key_grad(wl, 0, k, 0), n_s,
+                                                             wl.sigma_grad, idx0=r * S)
+    master = synth.normal_f32(wls.key_master(wl, 0), n_s, wl.sigma_master, idx0=r * S)
+    m = synth.normal_f32(wls.key_exp_avg(wl, 0), n_s, wl.sigma_state, idx0=r * S, absval=True)
+    v = synth.normal_f32(wls.key_exp_avg_sq(wl, 0), n_s, wl.sigma_state, idx0=r * S, absval=True)
+    others = [None if k == r else synth.normal_bf16(wls.key_shard(wl, 0), n_s, wl.sigma_master,
+                                                    idx0=k * S) for k in range(W)]
+    for i in range(args.warmup):
+        run_oracle_step(ora, grads, master, m, v, others, r, n_s, i + 1)
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        run_oracle_step(ora, grads, master, m, v, others, r, n_s, args.warmup + i + 1)
+    dt = time.perf_counter() - t0
+    per = (6 * W + 22) * n_s
+    value = per * args.steps / dt / 1e9
+    sample = ("unit 0 (one Llama block) of the Llama-7B local-rank workload, first %d elements of "
+              "rank 0's shard (W=8) per step" % n_s)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt * 1e3 / args.steps, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic",
+        "config": {"workload": "llama7b_local_rank", "W": W, "mode": "local-rank",
+                   "sample_elems_per_step": n_s},
+        "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default="llama7b")
+    ap.add_argument("--units", type=int, default=0, help="llama7b: only the first N units")
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--ref-sample", type=int, default=1 << 21)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        raise SystemExit("at least 3 warm-up steps")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,495 @@
+// GPU entry points of the C ABI (include/fsdp.h): argument validation, alias
+// checks, segment-table construction and launch of the segment kernel.
+//
+// Nothing here allocates device memory: each launch carries its descriptor
+// table as a __grid_constant__ kernel parameter.
+#include "fsdp.h"
+#include "segment_kernel.cuh"
+
+#include <algorithm>
+#include <atomic>
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <vector>
+
+namespace fsdp {
+namespace {
+
+// ------------------------------------------------------------ device facts
+
+constexpr int kMaxDevices = 64;
+constexpr int kNumVariants = 6;  // W = 1, 2, 4, 8, 16, generic
+
+std::atomic<int> g_sm_count[kMaxDevices];
+std::atomic<int> g_blocks_per_sm[kMaxDevices][kNumVariants];
+
+int variant_of(int w) {
+  switch (w) {
+    case 1: return 0;
+    case 2: return 1;
+    case 4: return 2;
+    case 8: return 3;
+    case 16: return 4;
+    default: return 5;
+  }
+}
+
+const void* kernel_of(int variant) {
+  switch (variant) {
+    case 0: return reinterpret_cast<const void*>(&segment_kernel<1>);
+    case 1: return reinterpret_cast<const void*>(&segment_kernel<2>);
+    case 2: return reinterpret_cast<const void*>(&segment_kernel<4>);
+    case 3: return reinterpret_cast<const void*>(&segment_kernel<8>);
+    case 4: return reinterpret_cast<const void*>(&segment_kernel<16>);
+    default: return reinterpret_cast<const void*>(&segment_kernel<0>);
+  }
+}
+
+// Resident-grid size for a kernel variant on the current device (cached).
+int grid_capacity(int variant, int* err) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+    *err = FSDP_ECUDA;
+    return 0;
+  }
+  int sms = g_sm_count[dev].load(std::memory_order_relaxed);
+  if (sms == 0) {
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0) {
+      *err = FSDP_ECUDA;
+      return 0;
+    }
+    g_sm_count[dev].store(sms, std::memory_order_relaxed);
+  }
+  int per_sm = g_blocks_per_sm[dev][variant].load(std::memory_order_relaxed);
+  if (per_sm == 0) {
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel_of(variant), kThreads, 0) !=
+            cudaSuccess ||
+        per_sm <= 0) {
+      *err = FSDP_ECUDA;
+      return 0;
+    }
+    g_blocks_per_sm[dev][variant].store(per_sm, std::memory_order_relaxed);
+  }
+  return sms * per_sm;
+}
+
+// ------------------------------------------------------------ segment table
+
+struct SegmentList {
+  std::vector<Seg> seg;
+  std::vector<const void*> ptr;
+
+  static bool aligned16(const void* q) { return (reinterpret_cast<uintptr_t>(q) & 15u) == 0; }
+
+  // kStep / kReduce / kAdam: `ptrs` in pool order; width 16 iff all are aligned.
+  void add_elementwise(SegKind kind, int64_t n, int nrep, const std::vector<const void*>& ptrs) {
+    if (n <= 0) return;
+    bool ok = true;
+    for (const void* q : ptrs) ok = ok && (q == nullptr || aligned16(q));
+    Seg d{};
+    d.n = n;
+    d.kind = kind;
+    d.nrep = nrep;
+    d.ptr = static_cast<int32_t>(ptr.size());
+    d.width = ok ? 16 : 0;
+    seg.push_back(d);
+    ptr.insert(ptr.end(), ptrs.begin(), ptrs.end());
+  }
+
+  void add_bytes(SegKind kind, const void* src, void* dst, int64_t bytes) {
+    if (bytes <= 0) return;
+    const uintptr_t a = reinterpret_cast<uintptr_t>(dst) | (src ? reinterpret_cast<uintptr_t>(src) : 0);
+    int width = 1;
+    if ((a & 15u) == 0) {
+      width = 16;  // a ragged tail is copied byte by byte
+    } else {
+      const uintptr_t b = a | static_cast<uintptr_t>(bytes);
+      width = (b & 7u) == 0 ? 8 : (b & 3u) == 0 ? 4 : (b & 1u) == 0 ? 2 : 1;
+    }
+    Seg d{};
+    d.n = bytes;
+    d.kind = kind;
+    d.ptr = static_cast<int32_t>(ptr.size());
+    d.width = width;
+    seg.push_back(d);
+    if (kind == kCopy) ptr.push_back(src);
+    ptr.push_back(dst);
+  }
+
+  int pool_size(size_t i) const {
+    const int32_t end = (i + 1 < seg.size()) ? seg[i + 1].ptr : static_cast<int32_t>(ptr.size());
+    return end - seg[i].ptr;
+  }
+};
+
+int64_t chunks_of(const Seg& d) {
+  const int64_t unit = (d.kind == kCopy || d.kind == kZero) ? kChunkBytes : kChunkElems;
+  return (d.n + unit - 1) / unit;
+}
+
+template <int W>
+cudaError_t launch_variant(const Params& p, int grid, cudaStream_t stream) {
+  segment_kernel<W><<<grid, kThreads, 0, stream>>>(p);
+  return cudaGetLastError();
+}
+
+// Launch the list, splitting it where a descriptor table would overflow. With
+// `count` set, nothing is launched and the number of launches is returned there.
+int launch(const SegmentList& list, const Scalars& s, cudaStream_t stream, int* count = nullptr) {
+  if (count) *count = 0;
+  if (list.seg.empty()) return FSDP_OK;
+  const int variant = variant_of(s.w);
+  int err = FSDP_OK;
+  const int cap = count ? 1 : grid_capacity(variant, &err);
+  if (err != FSDP_OK) return err;
+  static thread_local Params p;  // ~27 KB: keep it off the stack
+  size_t i = 0;
+  while (i < list.seg.size()) {
+    std::memset(&p, 0, sizeof(p));
+    p.s = s;
+    int nseg = 0, nptr = 0;
+    int64_t chunks = 0;
+    while (i < list.seg.size() && nseg < kMaxSeg) {
+      const int np = list.pool_size(i);
+      if (nptr + np > kMaxPtr) break;
+      Seg d = list.seg[i];
+      for (int k = 0; k < np; ++k) p.ptr[nptr + k] = list.ptr[d.ptr + k];
+      d.ptr = nptr;
+      chunks += chunks_of(d);
+      d.chunk_end = chunks;
+      p.seg[nseg++] = d;
+      nptr += np;
+      ++i;
+    }
+    p.nseg = nseg;
+    p.total_chunks = chunks;
+    if (count) {
+      ++*count;
+      continue;
+    }
+    const int grid = static_cast<int>(std::min<int64_t>(chunks, cap));
+    cudaError_t e;
+    switch (variant) {
+      case 0: e = launch_variant<1>(p, grid, stream); break;
+      case 1: e = launch_variant<2>(p, grid, stream); break;
+      case 2: e = launch_variant<4>(p, grid, stream); break;
+      case 3: e = launch_variant<8>(p, grid, stream); break;
+      case 4: e = launch_variant<16>(p, grid, stream); break;
+      default: e = launch_variant<0>(p, grid, stream); break;
+    }
+    if (e != cudaSuccess) return FSDP_ECUDA;
+  }
+  return FSDP_OK;
+}
+
+// ------------------------------------------------------------ validation
+
+bool layout_ok(const fsdp_layout_t* L) {
+  if (!L) return false;
+  const int64_t w = L->world_size;
+  if (w < 1 || w > FSDP_MAX_WORLD || L->shard_factor < 1 || w % L->shard_factor != 0) return false;
+  if (L->n_tensors < 1 || L->numel < 0) return false;
+  if (L->numel > INT64_MAX - w) return false;
+  if (L->padded_numel != (L->numel + w - 1) / w * w) return false;
+  return L->shard_numel * L->shard_factor == L->padded_numel;
+}
+
+int make_scalars(const fsdp_adam_t* h, int w, Scalars* s) {
+  if (!h) return FSDP_EINVAL;
+  if (h->step < 1 || h->weight_decay != 0.0) return FSDP_EINVAL;
+  if (!(h->beta1 >= 0.0 && h->beta1 < 1.0) || !(h->beta2 >= 0.0 && h->beta2 < 1.0)) return FSDP_EINVAL;
+  if (!(h->eps >= 0.0) || !std::isfinite(h->eps) || !std::isfinite(h->lr)) return FSDP_EINVAL;
+  const double t = static_cast<double>(h->step);
+  s->lr = static_cast<float>(h->lr);
+  s->b1 = static_cast<float>(h->beta1);
+  s->b2 = static_cast<float>(h->beta2);
+  s->eps = static_cast<float>(h->eps);
+  s->omb1 = static_cast<float>(1.0 - h->beta1);
+  s->omb2 = static_cast<float>(1.0 - h->beta2);
+  s->bc1 = static_cast<float>(1.0 - std::pow(h->beta1, t));
+  s->bc2 = static_cast<float>(1.0 - std::pow(h->beta2, t));
+  if (!(s->bc1 > 0.0f) || !(s->bc2 > 0.0f)) return FSDP_EINVAL;
+  s->w = w;
+  s->inv_w = (w > 0 && (w & (w - 1)) == 0) ? 1.0f / static_cast<float>(w) : 0.0f;
+  return FSDP_OK;
+}
+
+Scalars reduce_only_scalars(int w) {
+  Scalars s{};
+  s.w = w;
+  s.inv_w = (w & (w - 1)) == 0 ? 1.0f / static_cast<float>(w) : 0.0f;
+  return s;
+}
+
+// Byte ranges for overlap checks.
+struct Range {
+  uintptr_t lo, hi;
+};
+
+Range range_of(const void* p, int64_t bytes) {
+  const uintptr_t a = reinterpret_cast<uintptr_t>(p);
+  return Range{a, a + static_cast<uintptr_t>(bytes)};
+}
+
+class AliasCheck {
+ public:
+  void output(const void* p, int64_t bytes) {
+    if (bytes > 0) out_.push_back(range_of(p, bytes));
+  }
+  void input(const void* p, int64_t bytes) {
+    if (bytes > 0) in_.push_back(range_of(p, bytes));
+  }
+  // True when outputs are pairwise disjoint and no input overlaps an output.
+  bool ok() {
+    std::sort(out_.begin(), out_.end(), [](const Range& a, const Range& b) { return a.lo < b.lo; });
+    for (size_t i = 1; i < out_.size(); ++i)
+      if (out_[i].lo < out_[i - 1].hi) return false;
+    for (const Range& r : in_) {
+      // first output whose end lies beyond r.lo (outputs are disjoint, so ends are sorted too)
+      auto it = std::upper_bound(out_.begin(), out_.end(), r.lo,
+                                 [](uintptr_t v, const Range& o) { return v < o.hi; });
+      if (it != out_.end() && it->lo < r.hi) return false;
+    }
+    return true;
+  }
+
+ private:
+  std::vector<Range> out_, in_;
+};
+
+// Appends one unit's fused-step segments; checks pointers and aliasing.
+int build_unit(const fsdp_unit_args_t& u, int32_t rb, int32_t re, SegmentList& list,
+               AliasCheck& alias) {
+  const fsdp_layout_t* L = u.layout;
+  const int W = L->world_size, F = L->shard_factor, R = W / F;
+  const int64_t S = L->shard_numel, padded = L->padded_numel;
+  if (padded == 0) return FSDP_OK;
+  if (!u.grads || !u.master || !u.exp_avg || !u.exp_avg_sq || !u.full_out) return FSDP_EINVAL;
+  for (int k = 0; k < W; ++k) {
+    if (!u.grads[k]) return FSDP_EINVAL;
+    alias.input(u.grads[k], padded * 2);
+  }
+  // positions with at least one owned replica, each reduced once
+  std::vector<const void*> ptrs;
+  for (int p = 0; p < F; ++p) {
+    ptrs.clear();
+    for (int k = 0; k < W; ++k) ptrs.push_back(u.grads[k] + p * S);
+    int nrep = 0;
+    for (int g = 0; g < R; ++g) {
+      const int r = g * F + p;
+      if (r < rb || r >= re) continue;
+      const int o = r - rb;
+      float* mp = u.master[o];
+      float* mm = u.exp_avg[o];
+      float* mv = u.exp_avg_sq[o];
+      uint16_t* full = u.full_out[g];
+      if (!mp || !mm || !mv || !full) return FSDP_EINVAL;
+      alias.output(mp, S * 4);
+      alias.output(mm, S * 4);
+      alias.output(mv, S * 4);
+      ptrs.push_back(mp);
+      ptrs.push_back(mm);
+      ptrs.push_back(mv);
+      ptrs.push_back(full + p * S);
+      ++nrep;
+    }
+    if (nrep > 0) list.add_elementwise(kStep, S, nrep, ptrs);
+  }
+  // gather the non-owned positions of every group that holds an owned rank
+  for (int g = 0; g < R; ++g) {
+    const int lo = g * F, hi = lo + F;
+    if (hi <= rb || lo >= re) continue;
+    uint16_t* full = u.full_out[g];
+    alias.output(full, padded * 2);
+    for (int p = 0; p < F; ++p) {
+      const int r = lo + p;
+      if (r >= rb && r < re) continue;
+      if (!u.other_shards || !u.other_shards[r]) return FSDP_EINVAL;
+      const uint16_t* src = u.other_shards[r];
+      if (src == full + p * S) continue;  // already in place
+      alias.input(src, S * 2);
+      list.add_bytes(kCopy, src, full + p * S, S * 2);
+    }
+  }
+  return FSDP_OK;
+}
+
+}  // namespace
+}  // namespace fsdp
+
+using namespace fsdp;
+
+namespace {
+
+int grouped(const fsdp_unit_args_t* units, int32_t n_units, int32_t rank_begin, int32_t rank_end,
+            const fsdp_adam_t* adam, cudaStream_t stream, int* count) {
+  if (count) *count = 0;
+  if (n_units < 0 || (n_units > 0 && !units)) return FSDP_EINVAL;
+  if (n_units == 0) return FSDP_OK;
+  const fsdp_layout_t* L0 = units[0].layout;
+  if (!layout_ok(L0)) return FSDP_EINVAL;
+  const int W = L0->world_size, F = L0->shard_factor;
+  if (rank_begin < 0 || rank_end > W || rank_begin >= rank_end) return FSDP_EINVAL;
+  Scalars s{};
+  if (adam) {
+    if (int rc = make_scalars(adam, W, &s)) return rc;
+  } else {
+    if (!count) return FSDP_EINVAL;
+    s = reduce_only_scalars(W);
+  }
+  SegmentList list;
+  AliasCheck alias;
+  for (int32_t i = 0; i < n_units; ++i) {
+    const fsdp_layout_t* L = units[i].layout;
+    if (!layout_ok(L) || L->world_size != W || L->shard_factor != F) return FSDP_EINVAL;
+    if (int rc = build_unit(units[i], rank_begin, rank_end, list, alias)) return rc;
+  }
+  if (!alias.ok()) return FSDP_EALIAS;
+  return launch(list, s, stream, count);
+}
+
+}  // namespace
+
+extern "C" int fsdp_shard_step_grouped(const fsdp_unit_args_t* units, int32_t n_units,
+                                       int32_t rank_begin, int32_t rank_end,
+                                       const fsdp_adam_t* adam, fsdp_stream_t stream) {
+  return grouped(units, n_units, rank_begin, rank_end, adam, reinterpret_cast<cudaStream_t>(stream),
+                 nullptr);
+}
+
+extern "C" int fsdp_shard_step_grouped_launches(const fsdp_unit_args_t* units, int32_t n_units,
+                                                int32_t rank_begin, int32_t rank_end,
+                                                int32_t* launches_out) {
+  if (!launches_out) return FSDP_EINVAL;
+  int count = 0;
+  const int rc = grouped(units, n_units, rank_begin, rank_end, nullptr, nullptr, &count);
+  if (rc == FSDP_OK) *launches_out = count;
+  return rc;
+}
+
+extern "C" int fsdp_shard_step(const uint16_t* const* grads, const fsdp_layout_t* layout,
+                               int32_t rank_begin, int32_t rank_end, float* const* master,
+                               float* const* exp_avg, float* const* exp_avg_sq,
+                               const uint16_t* const* other_shards, uint16_t* const* full_out,
+                               const fsdp_adam_t* adam, fsdp_stream_t stream) {
+  fsdp_unit_args_t u{layout, grads, master, exp_avg, exp_avg_sq, other_shards, full_out};
+  return fsdp_shard_step_grouped(&u, 1, rank_begin, rank_end, adam, stream);
+}
+
+extern "C" int fsdp_reduce_scatter(const uint16_t* const* grads, const fsdp_layout_t* L,
+                                   int32_t rank, float* grad_shard_out, fsdp_stream_t stream) {
+  if (!layout_ok(L) || !grads || !grad_shard_out) return FSDP_EINVAL;
+  const int W = L->world_size, F = L->shard_factor;
+  if (rank < 0 || rank >= W) return FSDP_EINVAL;
+  const int64_t S = L->shard_numel;
+  if (S == 0) return FSDP_OK;
+  const int p = rank % F;
+  AliasCheck alias;
+  std::vector<const void*> ptrs;
+  for (int k = 0; k < W; ++k) {
+    if (!grads[k]) return FSDP_EINVAL;
+    alias.input(grads[k], L->padded_numel * 2);
+    ptrs.push_back(grads[k] + p * S);
+  }
+  alias.output(grad_shard_out, S * 4);
+  if (!alias.ok()) return FSDP_EALIAS;
+  ptrs.push_back(grad_shard_out);
+  SegmentList list;
+  list.add_elementwise(kReduce, S, 0, ptrs);
+  return launch(list, reduce_only_scalars(W), reinterpret_cast<cudaStream_t>(stream));
+}
+
+extern "C" int fsdp_adam_shard_step(float* master, float* exp_avg, float* exp_avg_sq,
+                                    const float* grad_shard, int64_t n, const fsdp_adam_t* adam,
+                                    uint16_t* bf16_shard_out, fsdp_stream_t stream) {
+  if (n < 0) return FSDP_EINVAL;
+  Scalars s{};
+  if (int rc = make_scalars(adam, 1, &s)) return rc;
+  if (n == 0) return FSDP_OK;
+  if (!master || !exp_avg || !exp_avg_sq || !grad_shard) return FSDP_EINVAL;
+  AliasCheck alias;
+  alias.output(master, n * 4);
+  alias.output(exp_avg, n * 4);
+  alias.output(exp_avg_sq, n * 4);
+  if (bf16_shard_out) alias.output(bf16_shard_out, n * 2);
+  alias.input(grad_shard, n * 4);
+  if (!alias.ok()) return FSDP_EALIAS;
+  SegmentList list;
+  list.add_elementwise(kAdam, n, 1, {grad_shard, master, exp_avg, exp_avg_sq, bf16_shard_out});
+  return launch(list, s, reinterpret_cast<cudaStream_t>(stream));
+}
+
+extern "C" int fsdp_all_gather(const uint16_t* const* shards, const fsdp_layout_t* L,
+                               uint16_t* full_out, fsdp_stream_t stream) {
+  if (!layout_ok(L) || !shards || !full_out) return FSDP_EINVAL;
+  const int F = L->shard_factor;
+  const int64_t S = L->shard_numel;
+  if (S == 0) return FSDP_OK;
+  AliasCheck alias;
+  alias.output(full_out, L->padded_numel * 2);
+  SegmentList list;
+  for (int k = 0; k < F; ++k) {
+    if (!shards[k]) return FSDP_EINVAL;
+    if (shards[k] == full_out + k * S) continue;
+    alias.input(shards[k], S * 2);
+    list.add_bytes(kCopy, shards[k], full_out + k * S, S * 2);
+  }
+  if (!alias.ok()) return FSDP_EALIAS;
+  return launch(list, reduce_only_scalars(1), reinterpret_cast<cudaStream_t>(stream));
+}
+
+namespace {
+
+int elem_size_of(int32_t dtype) {
+  return dtype == FSDP_DTYPE_F32 ? 4 : dtype == FSDP_DTYPE_BF16 ? 2 : 0;
+}
+
+bool offsets_ok(const fsdp_layout_t* L, const int64_t* offsets) {
+  if (!offsets || offsets[0] != 0 || offsets[L->n_tensors] != L->numel) return false;
+  for (int32_t t = 0; t < L->n_tensors; ++t)
+    if (offsets[t + 1] < offsets[t]) return false;
+  return true;
+}
+
+}  // namespace
+
+extern "C" int fsdp_pack_flat(const void* const* tensors, const fsdp_layout_t* L,
+                              const int64_t* offsets, int32_t dtype, void* flat_out,
+                              fsdp_stream_t stream) {
+  const int es = elem_size_of(dtype);
+  if (!layout_ok(L) || es == 0 || !tensors || !flat_out || !offsets_ok(L, offsets)) return FSDP_EINVAL;
+  auto* flat = static_cast<unsigned char*>(flat_out);
+  AliasCheck alias;
+  alias.output(flat, L->padded_numel * es);
+  SegmentList list;
+  for (int32_t t = 0; t < L->n_tensors; ++t) {
+    const int64_t bytes = (offsets[t + 1] - offsets[t]) * es;
+    if (bytes == 0) continue;
+    if (!tensors[t]) return FSDP_EINVAL;
+    alias.input(tensors[t], bytes);
+    list.add_bytes(kCopy, tensors[t], flat + offsets[t] * es, bytes);
+  }
+  list.add_bytes(kZero, nullptr, flat + L->numel * es, (L->padded_numel - L->numel) * es);
+  if (!alias.ok()) return FSDP_EALIAS;
+  return launch(list, reduce_only_scalars(1), reinterpret_cast<cudaStream_t>(stream));
+}
+
+extern "C" int fsdp_unpack_flat(const void* flat_in, const fsdp_layout_t* L, const int64_t* offsets,
+                                int32_t dtype, void* const* tensors_out, fsdp_stream_t stream) {
+  const int es = elem_size_of(dtype);
+  if (!layout_ok(L) || es == 0 || !tensors_out || !flat_in || !offsets_ok(L, offsets)) return FSDP_EINVAL;
+  const auto* flat = static_cast<const unsigned char*>(flat_in);
+  AliasCheck alias;
+  alias.input(flat, L->padded_numel * es);
+  SegmentList list;
+  for (int32_t t = 0; t < L->n_tensors; ++t) {
+    const int64_t bytes = (offsets[t + 1] - offsets[t]) * es;
+    if (bytes == 0) continue;
+    if (!tensors_out[t]) return FSDP_EINVAL;
+    alias.output(tensors_out[t], bytes);
+    list.add_bytes(kCopy, flat + offsets[t] * es, tensors_out[t], bytes);
+  }
+  if (!alias.ok()) return FSDP_EALIAS;
+  return launch(list, reduce_only_scalars(1), reinterpret_cast<cudaStream_t>(stream));
+}

@@ -1,0 +1,391 @@
+// Device code of the FSDP FlatParameter step for sm_103a.
+//
+// Every GPU entry point of the C ABI becomes a list of *segments* run by one
+// persistent, grid-strided kernel:
+//   kStep    reduce-scatter + Adam + bf16 cast for one shard position, with the
+//            reduced gradient applied to every replica that owns the position
+//            (the fused step; page "transformer math: FSDP", "The backward
+//            cycle: all-gather, grads, reduce-scatter")
+//   kReduce  reduce-scatter only (fp32 gradient shard out)
+//   kAdam    Adam + bf16 cast only
+//   kCopy    byte copy (all-gather of bf16 shards, pack, unpack; "The forward
+//            cycle: all-gather, compute, reshard")
+//   kZero    zero fill (FlatParameter padding)
+// A segment is cut into fixed-size chunks; chunk c of the whole launch is
+// processed by block c mod gridDim, so all resident blocks stream through the
+// same region of HBM together. The path is HBM-bound (no dense contraction,
+// ~10 fp32 operations per 42+ bytes), so the design goals are 16-byte
+// coalesced accesses, W independent gradient loads in flight per thread, and
+// streaming cache hints; no tensor cores.
+//
+// Arithmetic is bit-identical to the definition: fp32 left fold of the W bf16
+// gradients in rank order starting from +0, IEEE division by W (a multiply by
+// the exact reciprocal when W is a power of two, which rounds identically),
+// Adam with one rounding per operation (__f*_rn intrinsics: no contraction
+// into FMA), round-to-nearest-even bf16 cast.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace fsdp {
+
+constexpr int kThreads = 256;
+constexpr int kVec = 8;                                 // elements per thread per chunk
+constexpr int64_t kChunkElems = int64_t(kThreads) * kVec;  // 2048 elements
+constexpr int64_t kChunkBytes = int64_t(kThreads) * 16;    // 4096 bytes (copy / zero)
+
+enum SegKind : int32_t { kStep = 0, kReduce = 1, kAdam = 2, kCopy = 3, kZero = 4 };
+
+// One segment. Pointer pool layout (Params::ptr, starting at `ptr`):
+//   kStep   : W gradient rows (bf16, already offset to the position),
+//             then nrep x {master, exp_avg, exp_avg_sq, bf16 out}
+//   kReduce : W gradient rows, fp32 out
+//   kAdam   : fp32 grad, master, exp_avg, exp_avg_sq, bf16 out (may be null)
+//   kCopy   : src, dst          (n in bytes)
+//   kZero   : dst               (n in bytes)
+struct Seg {
+  int64_t n;          // elements (kStep/kReduce/kAdam) or bytes (kCopy/kZero)
+  int64_t chunk_end;  // running total of chunks up to and including this segment
+  int32_t kind;
+  int32_t nrep;       // kStep: replicas updated from the reduced gradient
+  int32_t ptr;        // first pool entry
+  int32_t width;      // kStep/kReduce/kAdam: 16 if every pointer is 16-byte aligned, else 0;
+                      // kCopy/kZero: access width in bytes (16, 8, 4, 2 or 1)
+};
+
+// Per-launch fp32 scalars (formed on the host in double, rounded once).
+struct Scalars {
+  float lr, b1, b2, eps;
+  float omb1, omb2;   // 1 - b1, 1 - b2
+  float bc1, bc2;     // 1 - b1^t, 1 - b2^t
+  float inv_w;        // 1 / W if W is a power of two (exact), else 0
+  int32_t w;          // W
+};
+
+constexpr int kMaxSeg = 320;
+constexpr int kMaxPtr = 2048;
+
+// Passed by value as a __grid_constant__ kernel parameter (~26.7 KB, within the
+// 32,764-byte limit): the whole descriptor table arrives with the launch, no
+// device allocation or copy is needed.
+struct Params {
+  Scalars s;
+  int32_t nseg;
+  int32_t reserved;
+  int64_t total_chunks;
+  Seg seg[kMaxSeg];
+  const void* ptr[kMaxPtr];
+};
+static_assert(sizeof(Params) <= 32764, "kernel parameter block too large");
+
+// ------------------------------------------------------------ memory access
+
+__device__ __forceinline__ uint4 ld_stream_u4(const void* p) {
+  return __ldcs(reinterpret_cast<const uint4*>(p));
+}
+__device__ __forceinline__ float4 ld_stream_f4(const float* p) {
+  return __ldcs(reinterpret_cast<const float4*>(p));
+}
+__device__ __forceinline__ void st_stream_f4(float* p, float4 v) {
+  __stcs(reinterpret_cast<float4*>(p), v);
+}
+__device__ __forceinline__ void st_stream_u4(void* p, uint4 v) {
+  __stcs(reinterpret_cast<uint4*>(p), v);
+}
+
+// ------------------------------------------------------------- arithmetic
+
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+__device__ __forceinline__ float bf16_to_f32(uint16_t h) {
+  return __uint_as_float(static_cast<uint32_t>(h) << 16);
+}
+__device__ __forceinline__ uint32_t bf16x2_rn(float lo, float hi) {
+  __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);  // .x = lo (low half), .y = hi
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+__device__ __forceinline__ uint16_t bf16_rn(float x) {
+  return __bfloat16_as_ushort(__float2bfloat16_rn(x));
+}
+
+// Mean over W of the folded sum.
+template <int W>
+__device__ __forceinline__ float mean_of(float acc, const Scalars& s) {
+  if constexpr (W > 0 && (W & (W - 1)) == 0) {
+    return __fmul_rn(acc, 1.0f / W);  // exact reciprocal: same rounding as acc / W
+  } else {
+    return s.inv_w != 0.0f ? __fmul_rn(acc, s.inv_w) : __fdiv_rn(acc, static_cast<float>(s.w));
+  }
+}
+
+// Adam (Kingma & Ba 2015, Algorithm 1, weight decay 0) on one element.
+__device__ __forceinline__ void adam1(float g, float& p, float& m, float& v, const Scalars& s) {
+  m = __fadd_rn(__fmul_rn(s.b1, m), __fmul_rn(s.omb1, g));
+  v = __fadd_rn(__fmul_rn(s.b2, v), __fmul_rn(s.omb2, __fmul_rn(g, g)));
+  const float m_hat = __fdiv_rn(m, s.bc1);
+  const float v_hat = __fdiv_rn(v, s.bc2);
+  const float denom = __fadd_rn(__fsqrt_rn(v_hat), s.eps);
+  p = __fsub_rn(p, __fmul_rn(s.lr, __fdiv_rn(m_hat, denom)));
+}
+
+__device__ __forceinline__ void add_bf16x8(float (&acc)[8], const uint4& r) {
+  acc[0] = __fadd_rn(acc[0], bf16_lo(r.x));
+  acc[1] = __fadd_rn(acc[1], bf16_hi(r.x));
+  acc[2] = __fadd_rn(acc[2], bf16_lo(r.y));
+  acc[3] = __fadd_rn(acc[3], bf16_hi(r.y));
+  acc[4] = __fadd_rn(acc[4], bf16_lo(r.z));
+  acc[5] = __fadd_rn(acc[5], bf16_hi(r.z));
+  acc[6] = __fadd_rn(acc[6], bf16_lo(r.w));
+  acc[7] = __fadd_rn(acc[7], bf16_hi(r.w));
+}
+
+// Reduced gradient of 8 consecutive elements at e: every row loaded first (W
+// independent 16-byte loads in flight), then folded in rank order.
+template <int W>
+__device__ __forceinline__ void fold8(const Params& p, const Seg& d, int64_t e, float (&g)[8]) {
+#pragma unroll
+  for (int i = 0; i < 8; ++i) g[i] = 0.0f;
+  if constexpr (W > 0) {
+    uint4 r[W];
+#pragma unroll
+    for (int k = 0; k < W; ++k)
+      r[k] = ld_stream_u4(static_cast<const uint16_t*>(p.ptr[d.ptr + k]) + e);
+#pragma unroll
+    for (int k = 0; k < W; ++k) add_bf16x8(g, r[k]);
+  } else {
+    const int w = p.s.w;
+    for (int k0 = 0; k0 < w; k0 += 8) {
+      uint4 r[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k)
+        if (k0 + k < w) r[k] = ld_stream_u4(static_cast<const uint16_t*>(p.ptr[d.ptr + k0 + k]) + e);
+#pragma unroll
+      for (int k = 0; k < 8; ++k)
+        if (k0 + k < w) add_bf16x8(g, r[k]);
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < 8; ++i) g[i] = mean_of<W>(g[i], p.s);
+}
+
+template <int W>
+__device__ __forceinline__ float fold1(const Params& p, const Seg& d, int64_t i) {
+  float acc = 0.0f;
+  const int w = W > 0 ? W : p.s.w;
+  for (int k = 0; k < w; ++k)
+    acc = __fadd_rn(acc, bf16_to_f32(static_cast<const uint16_t*>(p.ptr[d.ptr + k])[i]));
+  return mean_of<W>(acc, p.s);
+}
+
+struct State8 {
+  float p[8], m[8], v[8];
+};
+
+__device__ __forceinline__ void load_state8(State8& st, const float* mp, const float* mm,
+                                            const float* mv, int64_t e) {
+  const float4 p0 = ld_stream_f4(mp + e), p1 = ld_stream_f4(mp + e + 4);
+  const float4 m0 = ld_stream_f4(mm + e), m1 = ld_stream_f4(mm + e + 4);
+  const float4 v0 = ld_stream_f4(mv + e), v1 = ld_stream_f4(mv + e + 4);
+  st.p[0] = p0.x; st.p[1] = p0.y; st.p[2] = p0.z; st.p[3] = p0.w;
+  st.p[4] = p1.x; st.p[5] = p1.y; st.p[6] = p1.z; st.p[7] = p1.w;
+  st.m[0] = m0.x; st.m[1] = m0.y; st.m[2] = m0.z; st.m[3] = m0.w;
+  st.m[4] = m1.x; st.m[5] = m1.y; st.m[6] = m1.z; st.m[7] = m1.w;
+  st.v[0] = v0.x; st.v[1] = v0.y; st.v[2] = v0.z; st.v[3] = v0.w;
+  st.v[4] = v1.x; st.v[5] = v1.y; st.v[6] = v1.z; st.v[7] = v1.w;
+}
+
+__device__ __forceinline__ void store_state8(const State8& st, float* mp, float* mm, float* mv,
+                                             uint16_t* out, int64_t e) {
+  st_stream_f4(mp + e, make_float4(st.p[0], st.p[1], st.p[2], st.p[3]));
+  st_stream_f4(mp + e + 4, make_float4(st.p[4], st.p[5], st.p[6], st.p[7]));
+  st_stream_f4(mm + e, make_float4(st.m[0], st.m[1], st.m[2], st.m[3]));
+  st_stream_f4(mm + e + 4, make_float4(st.m[4], st.m[5], st.m[6], st.m[7]));
+  st_stream_f4(mv + e, make_float4(st.v[0], st.v[1], st.v[2], st.v[3]));
+  st_stream_f4(mv + e + 4, make_float4(st.v[4], st.v[5], st.v[6], st.v[7]));
+  if (out) {
+    uint4 o;
+    o.x = bf16x2_rn(st.p[0], st.p[1]);
+    o.y = bf16x2_rn(st.p[2], st.p[3]);
+    o.z = bf16x2_rn(st.p[4], st.p[5]);
+    o.w = bf16x2_rn(st.p[6], st.p[7]);
+    st_stream_u4(out + e, o);
+  }
+}
+
+// ------------------------------------------------------------- segment work
+
+template <int W>
+__device__ __forceinline__ void step_scalar(const Params& p, const Seg& d, int64_t i) {
+  const float g = fold1<W>(p, d, i);
+  const int w = W > 0 ? W : p.s.w;
+  for (int r = 0; r < d.nrep; ++r) {
+    const int b = d.ptr + w + 4 * r;
+    float* mp = static_cast<float*>(const_cast<void*>(p.ptr[b]));
+    float* mm = static_cast<float*>(const_cast<void*>(p.ptr[b + 1]));
+    float* mv = static_cast<float*>(const_cast<void*>(p.ptr[b + 2]));
+    uint16_t* out = static_cast<uint16_t*>(const_cast<void*>(p.ptr[b + 3]));
+    float pv = mp[i], mvv = mm[i], vv = mv[i];
+    adam1(g, pv, mvv, vv, p.s);
+    mp[i] = pv;
+    mm[i] = mvv;
+    mv[i] = vv;
+    out[i] = bf16_rn(pv);
+  }
+}
+
+template <int W>
+__device__ __forceinline__ void step_chunk(const Params& p, const Seg& d, int64_t e0) {
+  const int w = W > 0 ? W : p.s.w;
+  if (d.width == 16) {
+    const int64_t e = e0 + int64_t(threadIdx.x) * kVec;
+    if (e + kVec <= d.n) {
+      const int b0 = d.ptr + w;
+      State8 st;
+      // state of the first replica is requested before the gradient fold
+      load_state8(st, static_cast<const float*>(p.ptr[b0]), static_cast<const float*>(p.ptr[b0 + 1]),
+                  static_cast<const float*>(p.ptr[b0 + 2]), e);
+      float g[8];
+      fold8<W>(p, d, e, g);
+      for (int r = 0; r < d.nrep; ++r) {
+        const int b = b0 + 4 * r;
+        float* mp = static_cast<float*>(const_cast<void*>(p.ptr[b]));
+        float* mm = static_cast<float*>(const_cast<void*>(p.ptr[b + 1]));
+        float* mv = static_cast<float*>(const_cast<void*>(p.ptr[b + 2]));
+        uint16_t* out = static_cast<uint16_t*>(const_cast<void*>(p.ptr[b + 3]));
+        if (r > 0) load_state8(st, mp, mm, mv, e);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) adam1(g[i], st.p[i], st.m[i], st.v[i], p.s);
+        store_state8(st, mp, mm, mv, out, e);
+      }
+    } else {
+      for (int64_t i = e; i < d.n; ++i) step_scalar<W>(p, d, i);
+    }
+  } else {
+#pragma unroll 1
+    for (int k = 0; k < kVec; ++k) {
+      const int64_t i = e0 + int64_t(k) * kThreads + threadIdx.x;
+      if (i < d.n) step_scalar<W>(p, d, i);
+    }
+  }
+}
+
+template <int W>
+__device__ __forceinline__ void reduce_chunk(const Params& p, const Seg& d, int64_t e0) {
+  const int w = W > 0 ? W : p.s.w;
+  float* out = static_cast<float*>(const_cast<void*>(p.ptr[d.ptr + w]));
+  if (d.width == 16) {
+    const int64_t e = e0 + int64_t(threadIdx.x) * kVec;
+    if (e + kVec <= d.n) {
+      float g[8];
+      fold8<W>(p, d, e, g);
+      st_stream_f4(out + e, make_float4(g[0], g[1], g[2], g[3]));
+      st_stream_f4(out + e + 4, make_float4(g[4], g[5], g[6], g[7]));
+    } else {
+      for (int64_t i = e; i < d.n; ++i) out[i] = fold1<W>(p, d, i);
+    }
+  } else {
+#pragma unroll 1
+    for (int k = 0; k < kVec; ++k) {
+      const int64_t i = e0 + int64_t(k) * kThreads + threadIdx.x;
+      if (i < d.n) out[i] = fold1<W>(p, d, i);
+    }
+  }
+}
+
+__device__ __forceinline__ void adam_chunk(const Params& p, const Seg& d, int64_t e0) {
+  const float* gp = static_cast<const float*>(p.ptr[d.ptr]);
+  float* mp = static_cast<float*>(const_cast<void*>(p.ptr[d.ptr + 1]));
+  float* mm = static_cast<float*>(const_cast<void*>(p.ptr[d.ptr + 2]));
+  float* mv = static_cast<float*>(const_cast<void*>(p.ptr[d.ptr + 3]));
+  uint16_t* out = static_cast<uint16_t*>(const_cast<void*>(p.ptr[d.ptr + 4]));
+  if (d.width == 16) {
+    const int64_t e = e0 + int64_t(threadIdx.x) * kVec;
+    if (e + kVec <= d.n) {
+      State8 st;
+      load_state8(st, mp, mm, mv, e);
+      const float4 g0 = ld_stream_f4(gp + e), g1 = ld_stream_f4(gp + e + 4);
+      const float g[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
+#pragma unroll
+      for (int i = 0; i < 8; ++i) adam1(g[i], st.p[i], st.m[i], st.v[i], p.s);
+      store_state8(st, mp, mm, mv, out, e);
+      return;
+    }
+  }
+  const bool vec = d.width == 16;
+  const int64_t lo = vec ? e0 + int64_t(threadIdx.x) * kVec : 0;
+  for (int k = 0; k < kVec; ++k) {
+    const int64_t i = vec ? lo + k : e0 + int64_t(k) * kThreads + threadIdx.x;
+    if (i >= d.n) continue;
+    float pv = mp[i], mvv = mm[i], vv = mv[i];
+    adam1(gp[i], pv, mvv, vv, p.s);
+    mp[i] = pv;
+    mm[i] = mvv;
+    mv[i] = vv;
+    if (out) out[i] = bf16_rn(pv);
+  }
+}
+
+template <bool kZeroFill>
+__device__ __forceinline__ void bytes_chunk(const Params& p, const Seg& d, int64_t b0) {
+  const unsigned char* src =
+      kZeroFill ? nullptr : static_cast<const unsigned char*>(p.ptr[d.ptr]);
+  unsigned char* dst = static_cast<unsigned char*>(const_cast<void*>(p.ptr[d.ptr + (kZeroFill ? 0 : 1)]));
+  const int64_t end = (b0 + kChunkBytes < d.n) ? b0 + kChunkBytes : d.n;
+  switch (d.width) {
+    case 16: {
+      const int64_t b = b0 + int64_t(threadIdx.x) * 16;
+      if (b + 16 <= end) {
+        const uint4 v = kZeroFill ? make_uint4(0, 0, 0, 0) : ld_stream_u4(src + b);
+        st_stream_u4(dst + b, v);
+      } else {
+        for (int64_t i = b; i < end; ++i) dst[i] = kZeroFill ? 0 : src[i];
+      }
+      break;
+    }
+    case 8:
+      for (int64_t b = b0 + int64_t(threadIdx.x) * 8; b < end; b += int64_t(kThreads) * 8)
+        *reinterpret_cast<uint2*>(dst + b) =
+            kZeroFill ? make_uint2(0, 0) : *reinterpret_cast<const uint2*>(src + b);
+      break;
+    case 4:
+      for (int64_t b = b0 + int64_t(threadIdx.x) * 4; b < end; b += int64_t(kThreads) * 4)
+        *reinterpret_cast<uint32_t*>(dst + b) =
+            kZeroFill ? 0u : *reinterpret_cast<const uint32_t*>(src + b);
+      break;
+    case 2:
+      for (int64_t b = b0 + int64_t(threadIdx.x) * 2; b < end; b += int64_t(kThreads) * 2)
+        *reinterpret_cast<uint16_t*>(dst + b) =
+            kZeroFill ? uint16_t(0) : *reinterpret_cast<const uint16_t*>(src + b);
+      break;
+    default:
+      for (int64_t b = b0 + threadIdx.x; b < end; b += kThreads) dst[b] = kZeroFill ? 0 : src[b];
+      break;
+  }
+}
+
+// -------------------------------------------------------------- the kernel
+
+template <int W>
+__global__ void __launch_bounds__(kThreads) segment_kernel(const __grid_constant__ Params p) {
+  int s = 0;
+  int64_t first = 0;  // first chunk of segment s
+  for (int64_t c = blockIdx.x; c < p.total_chunks; c += gridDim.x) {
+    while (c >= p.seg[s].chunk_end) {
+      first = p.seg[s].chunk_end;
+      ++s;
+    }
+    const Seg& d = p.seg[s];
+    const int64_t local = c - first;
+    switch (d.kind) {
+      case kStep: step_chunk<W>(p, d, local * kChunkElems); break;
+      case kReduce: reduce_chunk<W>(p, d, local * kChunkElems); break;
+      case kAdam: adam_chunk(p, d, local * kChunkElems); break;
+      case kCopy: bytes_chunk<false>(p, d, local * kChunkBytes); break;
+      default: bytes_chunk<true>(p, d, local * kChunkBytes); break;
+    }
+  }
+}
+
+}  // namespace fsdp

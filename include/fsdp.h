@@ -1,0 +1,237 @@
+/*
+ * fsdp.h - C ABI of the GB300 FSDP FlatParameter shard step.
+ *
+ * One GPU holds W virtual data-parallel ranks. For one FSDP unit the step is:
+ * flatten the unit's tensors into one padded 1-D FlatParameter, reduce-scatter
+ * the W bf16 full gradients (fp32 sum in fixed rank order, divided by W),
+ * update each owned rank's fp32 master/exp_avg/exp_avg_sq shard with Adam in
+ * place, cast the result to bf16, and all-gather the bf16 shards into the full
+ * bf16 FlatParameter.
+ *
+ * Sources, cited by page title and section:
+ *   [notes] "NOTE-003: PyTorch FSDP" (reading notes on the FSDP paper)
+ *   [math]  "transformer math: FSDP"
+ *   [gloss] glossary entry "fully sharded data parallel fsdp"
+ *
+ * Conventions for every call:
+ *   - The caller owns all memory. The library allocates nothing and keeps no
+ *     state about the data between calls (it caches the SM count and kernel
+ *     occupancy per device).
+ *   - "device" pointers point to CUDA global memory of the current device;
+ *     pointer arrays themselves (const T* const*) are HOST arrays of device
+ *     pointers and are read before the call returns.
+ *   - bf16 values are passed as their uint16_t bit patterns; fp32 as float.
+ *   - Every GPU call is asynchronous on `stream` (0 = legacy default stream).
+ *     Inputs must stay unchanged, and outputs untouched, until the stream has
+ *     passed the call.
+ *   - Return value: FSDP_OK (0) or a negative status (below). All arguments
+ *     are validated on the host before anything is launched; on a negative
+ *     status nothing was launched (except FSDP_ECUDA from a failed launch).
+ *     Kernels never trap.
+ *   - Results are deterministic: the same inputs give bit-identical outputs.
+ *   - Sizes are int64_t element counts; all device index arithmetic is 64-bit.
+ */
+#ifndef FSDP_GB300_H
+#define FSDP_GB300_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t; declared here so the header needs no CUDA headers. */
+typedef struct CUstream_st *fsdp_stream_t;
+
+#define FSDP_OK 0
+#define FSDP_EINVAL (-1) /* null pointer, bad size, W outside [1,64], F not dividing W,
+                            rank outside [0,W), inconsistent layout, step < 1,
+                            weight_decay != 0, ... */
+#define FSDP_EALIAS (-2) /* an output overlaps an input or another output */
+#define FSDP_ECUDA (-3)  /* a CUDA launch failed (cudaGetLastError) */
+
+#define FSDP_MAX_WORLD 64
+
+#define FSDP_DTYPE_F32 0  /* 4-byte elements (fp32 master) */
+#define FSDP_DTYPE_BF16 1 /* 2-byte elements (bf16 bits) */
+
+/* Layout of one FlatParameter. [math] "The sharding unit: FlatParameter and the
+ * wrapping policy": the unit's tensors are flattened into one 1-D buffer that is
+ * split evenly over the ranks, each rank holding one contiguous slice.
+ * [notes] "Key results": sharding factor F (F = W full shard, F = 1 DDP,
+ * 1 < F < W hybrid). */
+typedef struct {
+  int64_t numel;        /* P: real elements (sum of tensor numels) */
+  int64_t padded_numel; /* ceil(P / W) * W: zero padding at the end */
+  int64_t shard_numel;  /* S = padded_numel / F: one rank's slice */
+  int32_t world_size;   /* W, 1..64 */
+  int32_t shard_factor; /* F, divides W; R = W / F replica groups */
+  int32_t n_tensors;
+} fsdp_layout_t;
+
+/* Adam hyper-parameters (Kingma & Ba 2015, Algorithm 1; the pages name the
+ * optimizer only: [math] "Why FSDP exists", [gloss] "Optimizer Step").
+ * Each per-element fp32 scalar (lr, beta1, beta2, eps, 1-beta1, 1-beta2,
+ * 1-beta1^step, 1-beta2^step) is formed in double and rounded once to fp32. */
+typedef struct {
+  double lr;
+  double beta1;        /* in [0, 1) */
+  double beta2;        /* in [0, 1) */
+  double eps;          /* >= 0, added outside the square root */
+  double weight_decay; /* must be 0 (the method uses none) */
+  int64_t step;        /* t >= 1: the step being taken */
+} fsdp_adam_t;
+
+/* a1. Flatten layout (host only, no GPU).
+ * [math] "The sharding unit: FlatParameter and the wrapping policy".
+ * numels: n_tensors element counts (>= 0) in the order the tensors are packed
+ * (row-major, concatenated, no padding between tensors).
+ * offsets_out: caller-owned array of n_tensors + 1 entries; offsets_out[i] is
+ * tensor i's first flat element, offsets_out[n_tensors] = P.
+ * out: the layout. Padding is to a multiple of W for every F, so the layout is
+ * the same for all sharding factors. EINVAL: n_tensors < 1, a negative numel,
+ * W outside [1,64], F < 1 or F not dividing W, a null pointer. */
+int fsdp_flatten_layout(const int64_t *numels, int32_t n_tensors, int32_t world_size,
+                        int32_t shard_factor, int64_t *offsets_out, fsdp_layout_t *out);
+
+/* a2. Pack tensors into the flat buffer (one launch), zero-filling the pad.
+ * tensors: host array of n_tensors device pointers (contiguous tensors of the
+ * element type `dtype`); offsets: the host array fsdp_flatten_layout wrote;
+ * flat_out: device buffer of padded_numel elements. Pad elements become +0.0
+ * (all-zero bits). EALIAS if flat_out overlaps a tensor. */
+int fsdp_pack_flat(const void *const *tensors, const fsdp_layout_t *layout,
+                   const int64_t *offsets, int32_t dtype, void *flat_out, fsdp_stream_t stream);
+
+/* a2. Unpack: copy each tensor's range of the flat buffer back out (pad dropped). */
+int fsdp_unpack_flat(const void *flat, const fsdp_layout_t *layout, const int64_t *offsets,
+                     int32_t dtype, void *const *tensors_out, fsdp_stream_t stream);
+
+/* a3. Reduce-scatter for one rank.
+ * [math] "The backward cycle: all-gather, grads, reduce-scatter"; [gloss]
+ * "Mixed Precision" (reduce_dtype fp32).
+ * grads: host array of W device pointers, grads[k] = rank k's bf16 full
+ * gradient, padded_numel elements (pad elements are expected to be zero).
+ * rank: in [0, W); it keeps position p = rank mod F, i.e. elements [p*S, (p+1)*S).
+ * grad_shard_out: device fp32 [S]:
+ *   out[j] = ((((0 + g_0[pS+j]) + g_1[pS+j]) + ... ) + g_{W-1}[pS+j]) / W
+ * a left fold in rank order over all W ranks, one fp32 rounding per add, IEEE
+ * division. EALIAS if the output overlaps a gradient row. */
+int fsdp_reduce_scatter(const uint16_t *const *grads, const fsdp_layout_t *layout,
+                        int32_t rank, float *grad_shard_out, fsdp_stream_t stream);
+
+/* a4 + a5. Adam on one shard, in place, and its bf16 cast.
+ * [math] "Why FSDP exists" (fp32 master, fp32 momentum and variance) and "The
+ * backward cycle" (the optimizer updates the local slice in place).
+ * master, exp_avg, exp_avg_sq: device fp32 [n], updated in place:
+ *   m = b1 m + (1-b1) g;  v = b2 v + (1-b2) g*g;
+ *   p = p - lr * ((m / (1-b1^t)) / (sqrt(v / (1-b2^t)) + eps))
+ * every operation one fp32 rounding (no fused multiply-add).
+ * grad_shard: device fp32 [n] (read only). bf16_shard_out: device bf16 [n],
+ * round-to-nearest-even of the new master, or NULL for none. n >= 0. */
+int fsdp_adam_shard_step(float *master, float *exp_avg, float *exp_avg_sq,
+                         const float *grad_shard, int64_t n, const fsdp_adam_t *adam,
+                         uint16_t *bf16_shard_out, fsdp_stream_t stream);
+
+/* a6. All-gather (unshard) one group.
+ * [math] "The forward cycle: all-gather, compute, reshard".
+ * shards: host array of F device pointers, shards[k] = bf16 [S] of position k;
+ * full_out: device bf16 [padded_numel]; full_out[k*S + j] = shards[k][j].
+ * A shard that already is the view full_out + k*S is left in place. */
+int fsdp_all_gather(const uint16_t *const *shards, const fsdp_layout_t *layout,
+                    uint16_t *full_out, fsdp_stream_t stream);
+
+/* a7 / a8. Fused shard step of one unit for the owned ranks [rank_begin, rank_end):
+ * reduce-scatter -> Adam -> bf16 cast -> all-gather in one launch, with no fp32
+ * gradient written to memory.
+ * Rank r belongs to group g = r / F (contiguous ranks form a group) at position
+ * p = r mod F ([gloss] "Hybrid Sharding", "HSDP": shard within a group,
+ * replicate across groups).
+ *   grads:        W device pointers, bf16 [padded_numel] each (as in a3). For
+ *                 every F all W ranks are summed in global rank order, so every
+ *                 F gives bit-identical parameters.
+ *   master, exp_avg, exp_avg_sq:
+ *                 rank_end - rank_begin device pointers, fp32 [S] each, indexed
+ *                 by r - rank_begin; updated in place (a4).
+ *   other_shards: NULL when every group that contains an owned rank is fully
+ *                 owned (all-ranks mode); otherwise W device pointers indexed by
+ *                 rank, bf16 [S]: the already-updated shards of the non-owned
+ *                 ranks in those groups (local-rank mode; entries of owned
+ *                 ranks and of other groups are ignored and may be NULL).
+ *   full_out:     R = W / F device pointers indexed by group, bf16 [padded_numel];
+ *                 every group containing an owned rank is written completely:
+ *                 owned positions with the new bf16 shard, the others copied
+ *                 from other_shards (skipped when other_shards[r] already is
+ *                 full_out[g] + p*S). Entries of other groups are ignored.
+ * Positions owned by several replicas are reduced once and the result applied
+ * to every replica. EALIAS: an output overlaps an input or another output.
+ * padded_numel == 0 is a no-op. */
+int fsdp_shard_step(const uint16_t *const *grads, const fsdp_layout_t *layout,
+                    int32_t rank_begin, int32_t rank_end, float *const *master,
+                    float *const *exp_avg, float *const *exp_avg_sq,
+                    const uint16_t *const *other_shards, uint16_t *const *full_out,
+                    const fsdp_adam_t *adam, fsdp_stream_t stream);
+
+/* Arguments of one unit for fsdp_shard_step_grouped (same meaning as above). */
+typedef struct {
+  const fsdp_layout_t *layout;
+  const uint16_t *const *grads;
+  float *const *master;
+  float *const *exp_avg;
+  float *const *exp_avg_sq;
+  const uint16_t *const *other_shards;
+  uint16_t *const *full_out;
+} fsdp_unit_args_t;
+
+/* a7 over several units (e.g. one per transformer block, [math] "The sharding
+ * unit": transformer_auto_wrap_policy makes each block a unit) in one launch
+ * when they fit the launch's descriptor table, else in as few as needed.
+ * All units share W, F, the owned rank range and the hyper-parameters. Units
+ * must not share output memory. n_units == 0 is a no-op. */
+int fsdp_shard_step_grouped(const fsdp_unit_args_t *units, int32_t n_units, int32_t rank_begin,
+                            int32_t rank_end, const fsdp_adam_t *adam, fsdp_stream_t stream);
+
+/* Host only: the number of kernel launches fsdp_shard_step_grouped would make
+ * for these arguments (validated exactly as the call validates them; nothing is
+ * launched). *launches_out is written on FSDP_OK. */
+int fsdp_shard_step_grouped_launches(const fsdp_unit_args_t *units, int32_t n_units,
+                                     int32_t rank_begin, int32_t rank_end,
+                                     int32_t *launches_out);
+
+/* a9. Closed-form accountant (host only).
+ * [math] "Why FSDP exists": ~16 bytes per parameter (bf16 weight + bf16 grad +
+ * fp32 master + two fp32 Adam moments); DDP keeps 16P on every GPU.
+ * [math] "Per-unit memory and communication, in numbers":
+ *   persistent = 16 P / N, transient = 2 U (1 + prefetch); a ring all-gather or
+ *   reduce-scatter moves ~P per rank, an all-reduce ~2P; FSDP pays
+ *   AG(fwd) + AG(bwd) + RS(bwd) ~ 3P against DDP's ~2P; bf16 on the wire.
+ * With sharding factor F over N ranks (R = N / F groups): persistent 16 P / F;
+ * the three collectives run inside a group and the gradient slice P/F is
+ * all-reduced across the R groups:
+ *   comm_elems_ring = 3 (F-1)/F P + 2 (R-1)/R P/F
+ *   comm_elems      = 3P [F > 1] + 2 P/F [R > 1]   (the pages' rounded form)
+ * P, U: total parameters and parameters of the largest unit; prefetch >= 0
+ * units gathered ahead. EINVAL: N < 1, F < 1, F not dividing N, negatives. */
+typedef struct {
+  double persistent_bytes;     /* 16 P / F */
+  double ddp_persistent_bytes; /* 16 P */
+  double transient_bytes;      /* 2 U (1 + prefetch) */
+  double peak_bytes;           /* persistent + transient */
+  double comm_elems;           /* per rank per step, rounded form */
+  double comm_elems_ring;      /* per rank per step, exact ring form */
+  double ddp_comm_elems;       /* 2P */
+  double ddp_comm_elems_ring;  /* 2 (N-1)/N P */
+  double comm_bytes;           /* 2 bytes per element */
+  double ddp_comm_bytes;
+} fsdp_account_t;
+
+int fsdp_account(double P, double U, int32_t N, int32_t F, int32_t prefetch,
+                 fsdp_account_t *out);
+
+/* Text of a status code (static storage). */
+const char *fsdp_status_string(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FSDP_GB300_H */

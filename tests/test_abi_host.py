@@ -1,0 +1,227 @@
+"""C ABI host logic without a GPU: exported symbols, layout, accountant, argument checks.
+
+Every GPU entry point called here is given arguments that the host-side
+validation rejects, so no kernel is ever launched (the pointers are fake).
+"""
+import ctypes
+import glob
+import os
+import re
+
+import numpy as np
+import pytest
+
+import fully_sharded_gb300 as fs
+import oracle_pins as pins
+from fully_sharded_gb300 import FsdpError
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def declared_functions():
+    names = set()
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        text = open(h).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        names |= set(re.findall(r"\b(fsdp_\w+)\s*\(", text))
+    return sorted(names)
+
+
+def test_library_exports_every_declared_symbol():
+    names = declared_functions()
+    assert len(names) >= 10
+    lib = ctypes.CDLL(fs.library_path())
+    missing = [n for n in names if not hasattr(lib, n)]
+    assert not missing, missing
+
+
+def test_layout_matches_oracle_brute(ora):
+    rng = np.random.default_rng(0)
+    for W in range(1, 17):
+        for P in list(range(0, 40)) + [1000, 1000003]:
+            numels = [P] if P < 3 else np.diff(
+                np.concatenate([[0], np.sort(rng.integers(0, P + 1, size=3)), [P]])).tolist()
+            for F in [f for f in range(1, W + 1) if W % f == 0]:
+                lay, offs = fs.fsdp_flatten_layout(numels, W, F)
+                o_offs, oP, opad, oS = ora.flatten_layout(numels, W, F)
+                assert offs == o_offs.tolist()
+                assert (lay.numel, lay.padded_numel, lay.shard_numel) == (oP, opad, oS)
+                assert (lay.world_size, lay.shard_factor, lay.n_tensors) == (W, F, len(numels))
+
+
+def test_layout_golden_workloads():
+    for c in pins.golden("workload_layouts.json")["cases"]:
+        lay, offs = fs.fsdp_flatten_layout(c["numels"], c["W"], c["F"])
+        assert (lay.numel, lay.padded_numel, lay.shard_numel) == (c["P"], c["padded"], c["S"])
+        if c["offsets"] is not None:
+            assert offs == c["offsets"]
+
+
+@pytest.mark.parametrize("args", [
+    ([], 4, 4),          # no tensors
+    ([5], 0, 1),         # W < 1
+    ([5], 65, 65),       # W > 64
+    ([5], 8, 3),         # F does not divide W
+    ([5], 8, 0),         # F < 1
+    ([5, -1], 4, 4),     # negative numel
+    ([2**62, 2**62], 4, 4),  # overflow
+])
+def test_layout_rejects(args):
+    with pytest.raises(FsdpError) as e:
+        fs.fsdp_flatten_layout(*args)
+    assert e.value.status == fs.FSDP_EINVAL
+
+
+def test_account_matches_oracle(ora):
+    for P in (0.0, 1.0, 7e9, 124439808.0, 6738415616.0):
+        for N in (1, 2, 8, 16, 64):
+            for F in [f for f in range(1, N + 1) if N % f == 0]:
+                for pf in (0, 1, 2):
+                    a = fs.fsdp_account(P, P / 32, N, F, pf)
+                    b = ora.account(P, P / 32, N, F, pf)
+                    for k in b:
+                        assert a[k] == pytest.approx(b[k], rel=1e-13, abs=1e-6), (P, N, F, pf, k)
+
+
+def test_account_worked_example():
+    g = pins.golden("worked_example_7b.json")
+    i, e = g["inputs"], g["expected"]
+    a = fs.fsdp_account(i["P"], i["unit_params_printed"], i["N"], i["N"], i["prefetch"])
+    assert a["persistent_bytes"] == e["persistent_bytes"]
+    assert a["ddp_persistent_bytes"] == e["ddp_state_bytes"]
+    assert round(a["transient_bytes"] / 1e9, 1) == e["transient_bytes_1dec_gb"]
+    assert round(a["peak_bytes"] / 1e9) == e["peak_bytes_int_gb"]
+    assert a["comm_bytes"] == e["fsdp_comm_bytes"] and a["ddp_comm_bytes"] == e["ddp_comm_bytes"]
+
+
+def test_account_rejects():
+    for args in ((1e9, 1e8, 0, 1), (1e9, 1e8, 8, 3), (-1.0, 1.0, 8, 8), (1e9, 1e8, 8, 0)):
+        with pytest.raises(FsdpError):
+            fs.fsdp_account(*args)
+
+
+def test_status_strings():
+    assert fs.fsdp_status_string(0) == "ok"
+    for s in (fs.FSDP_EINVAL, fs.FSDP_EALIAS, fs.FSDP_ECUDA):
+        assert fs.fsdp_status_string(s) not in ("ok", "unknown status")
+
+
+# ---------------------------------------------- GPU entry points, rejected
+
+BASE = 1 << 40  # fake device addresses; every call below fails validation first
+HP = fs.AdamHyper()
+
+
+def _lay(P, W, F=None):
+    return fs.fsdp_flatten_layout([P], W, F)[0]
+
+
+def _expect(status, fn, *a, **k):
+    with pytest.raises(FsdpError) as e:
+        fn(*a, stream=0, **k)
+    assert e.value.status == status
+
+
+def _addr(i, size=1 << 24):
+    return BASE + i * size
+
+
+def test_shard_step_rejects_bad_arguments():
+    W = 4
+    lay = _lay(1024, W)
+    g = [_addr(k) for k in range(W)]
+    st = lambda j: [_addr(10 + 3 * r + j) for r in range(W)]  # noqa: E731
+    full = [_addr(40)]
+    ok = dict(grads=g, layout=lay, rank_begin=0, rank_end=W, master=st(0), exp_avg=st(1),
+              exp_avg_sq=st(2), other_shards=None, full_out=full)
+
+    def call(status, **over):
+        a = dict(ok)
+        a.update(over)
+        _expect(status, fs.fsdp_shard_step, a["grads"], a["layout"], a["rank_begin"],
+                a["rank_end"], a["master"], a["exp_avg"], a["exp_avg_sq"], a["other_shards"],
+                a["full_out"], over.get("adam", HP))
+
+    call(fs.FSDP_EINVAL, rank_begin=2, rank_end=2)
+    call(fs.FSDP_EINVAL, rank_begin=-1)
+    call(fs.FSDP_EINVAL, rank_end=W + 1)
+    call(fs.FSDP_EINVAL, grads=g[:3] + [None])
+    call(fs.FSDP_EINVAL, master=st(0)[:3] + [None])
+    call(fs.FSDP_EINVAL, full_out=[None])
+    call(fs.FSDP_EINVAL, adam=fs.AdamHyper(step=0))
+    call(fs.FSDP_EINVAL, adam=fs.AdamHyper(weight_decay=0.01))
+    call(fs.FSDP_EINVAL, adam=fs.AdamHyper(beta1=1.0))
+    call(fs.FSDP_EINVAL, adam=fs.AdamHyper(beta2=-0.1))
+    call(fs.FSDP_EINVAL, adam=fs.AdamHyper(eps=-1.0))
+    call(fs.FSDP_EINVAL, adam=fs.AdamHyper(lr=float("nan")))
+    bad = fs.Layout(lay.numel, lay.padded_numel + W, lay.shard_numel, W, W, 1)
+    call(fs.FSDP_EINVAL, layout=bad)
+    bad = fs.Layout(lay.numel, lay.padded_numel, lay.shard_numel, W, 3, 1)
+    call(fs.FSDP_EINVAL, layout=bad)
+    # local-rank mode without the other shards
+    call(fs.FSDP_EINVAL, rank_begin=1, rank_end=2, master=st(0)[:1], exp_avg=st(1)[:1],
+         exp_avg_sq=st(2)[:1])
+    # outputs overlapping inputs or each other
+    call(fs.FSDP_EALIAS, master=[g[0]] + st(0)[1:])
+    call(fs.FSDP_EALIAS, exp_avg=st(0))
+    call(fs.FSDP_EALIAS, full_out=[g[3] + 2])
+    call(fs.FSDP_EALIAS, master=st(0)[:3] + [st(0)[2] + 4])
+
+
+def test_unfused_entry_points_reject_bad_arguments():
+    W = 4
+    lay = _lay(1000, W)
+    g = [_addr(k) for k in range(W)]
+    _expect(fs.FSDP_EINVAL, fs.fsdp_reduce_scatter, g, lay, W, _addr(20))
+    _expect(fs.FSDP_EINVAL, fs.fsdp_reduce_scatter, g, lay, -1, _addr(20))
+    _expect(fs.FSDP_EINVAL, fs.fsdp_reduce_scatter, g[:3] + [None], lay, 0, _addr(20))
+    _expect(fs.FSDP_EALIAS, fs.fsdp_reduce_scatter, g, lay, 0, g[1] + 100)
+    a = [_addr(30 + j) for j in range(5)]
+    _expect(fs.FSDP_EINVAL, fs.fsdp_adam_shard_step, a[0], a[1], a[2], a[3], fs.AdamHyper(step=0), n=10)
+    _expect(fs.FSDP_EINVAL, fs.fsdp_adam_shard_step, a[0], a[1], a[2], a[3], HP, n=-1)
+    _expect(fs.FSDP_EINVAL, fs.fsdp_adam_shard_step, a[0], a[1], None, a[3], HP, n=10)
+    _expect(fs.FSDP_EALIAS, fs.fsdp_adam_shard_step, a[0], a[0] + 8, a[2], a[3], HP, n=10)
+    _expect(fs.FSDP_EALIAS, fs.fsdp_adam_shard_step, a[0], a[1], a[2], a[2] + 4, HP, n=10)
+    _expect(fs.FSDP_EALIAS, fs.fsdp_adam_shard_step, a[0], a[1], a[2], a[3], HP,
+            bf16_shard_out=a[0] + 16, n=10)
+    sh = [_addr(50 + k) for k in range(W)]
+    _expect(fs.FSDP_EINVAL, fs.fsdp_all_gather, sh[:3] + [None], lay, _addr(60))
+    _expect(fs.FSDP_EALIAS, fs.fsdp_all_gather, sh[:3] + [_addr(60) + 2], lay, _addr(60))
+
+
+def test_pack_unpack_reject_bad_arguments():
+    lay, offs = fs.fsdp_flatten_layout([10, 20, 30], 4)
+    ts = [_addr(k) for k in range(3)]
+    lib = fs._lib
+
+    def pack(tensors, offsets, flat_addr, dtype=fs.FSDP_DTYPE_F32):
+        return lib.fsdp_pack_flat(fs._parray(tensors), ctypes.byref(lay), fs._offsets(offsets),
+                                  dtype, flat_addr, None)
+
+    def unpack(flat_addr, offsets, tensors, dtype=fs.FSDP_DTYPE_F32):
+        return lib.fsdp_unpack_flat(flat_addr, ctypes.byref(lay), fs._offsets(offsets), dtype,
+                                    fs._parray(tensors), None)
+
+    assert pack(ts, offs, _addr(9), dtype=7) == fs.FSDP_EINVAL
+    assert pack(ts, [1] + offs[1:], _addr(9)) == fs.FSDP_EINVAL
+    assert pack(ts, offs[:-1] + [offs[-1] + 1], _addr(9)) == fs.FSDP_EINVAL
+    assert pack(ts, [0, 20, 10, 60], _addr(9)) == fs.FSDP_EINVAL
+    assert pack(ts[:2] + [None], offs, _addr(9)) == fs.FSDP_EINVAL
+    assert pack(ts, offs, ts[1] + 8) == fs.FSDP_EALIAS
+    assert unpack(_addr(9), offs, ts[:2] + [None]) == fs.FSDP_EINVAL
+    assert unpack(_addr(9), offs, [ts[0], ts[0] + 4, ts[2]]) == fs.FSDP_EALIAS
+    assert unpack(_addr(9), offs, [ts[0], _addr(9) + 4, ts[2]]) == fs.FSDP_EALIAS
+
+
+def test_grouped_rejects_mixed_layouts():
+    l4 = _lay(1024, 4)
+    l8 = _lay(1024, 8)
+    u = lambda lay, i: dict(layout=lay, grads=[_addr(i * 100 + k) for k in range(lay.world_size)],  # noqa: E731
+                            master=[_addr(i * 100 + 20 + r) for r in range(lay.world_size)],
+                            exp_avg=[_addr(i * 100 + 40 + r) for r in range(lay.world_size)],
+                            exp_avg_sq=[_addr(i * 100 + 60 + r) for r in range(lay.world_size)],
+                            other_shards=None, full_out=[_addr(i * 100 + 90)])
+    _expect(fs.FSDP_EINVAL, fs.fsdp_shard_step_grouped, [u(l4, 0), u(l8, 1)], 0, 4, HP)
+    a, b = u(l4, 0), u(l4, 1)
+    b["full_out"] = [a["full_out"][0] + 64]  # two units writing the same full buffer
+    _expect(fs.FSDP_EALIAS, fs.fsdp_shard_step_grouped, [a, b], 0, 4, HP)

@@ -1,0 +1,161 @@
+"""Full-size workloads, in the launch configuration the benchmark times, checked on samples.
+
+Inputs are filled on the device by the seeded generator; the host regenerates
+the inputs at sampled positions (first/last elements of every shard, chunk and
+tensor boundaries, random positions), the oracle computes those outputs one by
+one, and they must equal the device outputs bit for bit. The hybrid workload
+is also checked for bit-identical parameters across F = 1, 4, 16 on every
+element.
+"""
+import numpy as np
+import pytest
+
+import gpu_util as gu
+import synth
+from synth import workloads as wls
+
+pytestmark = pytest.mark.gpu
+
+fs = pytest.importorskip("fully_sharded_gb300")
+bench = pytest.importorskip("bench")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _cuda():
+    torch = pytest.importorskip("torch")
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA GPU")
+    yield
+    torch.cuda.empty_cache()
+
+
+def sample_positions(n, offsets_in_shard=(), k=384, seed=0):
+    rng = np.random.default_rng(seed)
+    pts = set(range(min(n, 40))) | set(range(max(0, n - 40), n))
+    for b in (2047, 2048, 2049, 4095, 4096):
+        if b < n:
+            pts.add(b)
+    for o in offsets_in_shard:
+        for d in (-1, 0, 1):
+            if 0 <= o + d < n:
+                pts.add(o + d)
+    pts |= set(rng.integers(0, n, size=min(k, n)).tolist())
+    return np.array(sorted(pts), dtype=np.int64)
+
+
+def gather(t, idx):
+    torch = gu.torch()
+    return gu.to_host(t[torch.from_numpy(idx).cuda()])
+
+
+def oracle_at(ora, grad_rows, master, m, v, step):
+    """Oracle outputs for compact gathered inputs: fold over ranks, then Adam."""
+    g = ora.fold_mean(grad_rows)
+    p, mm, vv = master.copy(), m.copy(), v.copy()
+    bf = ora.adam(p, mm, vv, g, step=step, **gu.HP)
+    return p, mm, vv, bf
+
+
+def check_all_ranks_unit(ora, wl, u, unit, F, before, step, seed):
+    """Sampled parity for one all-ranks unit; `before` holds host draws of the inputs."""
+    lay = unit["layout"]
+    W, S, P = lay.world_size, lay.shard_numel, lay.numel
+    R = W // F
+    for p in range(F):
+        j = sample_positions(S, seed=seed + p)
+        i = p * S + j
+        rows = [synth.normal_bf16_at(wls.key_grad(wl, u, k, 0), i, wl.sigma_grad, n_valid=P) for k in range(W)]
+        master = synth.normal_f32_at(wls.key_master(wl, u), i, wl.sigma_master, n_valid=P)
+        if wl.sigma_state:
+            m = synth.normal_f32_at(wls.key_exp_avg(wl, u), i, wl.sigma_state, absval=True, n_valid=P)
+            v = synth.normal_f32_at(wls.key_exp_avg_sq(wl, u), i, wl.sigma_state, absval=True, n_valid=P)
+        else:
+            m = np.zeros(j.size, np.float32)
+            v = np.zeros(j.size, np.float32)
+        op, om, ov, obf = oracle_at(ora, rows, master, m, v, step)
+        for g in range(R):
+            r = g * F + p
+            gu.assert_same_bits(gather(unit["master"][r], j), op, "master u%d r%d" % (u, r))
+            gu.assert_same_bits(gather(unit["exp_avg"][r], j), om, "exp_avg u%d r%d" % (u, r))
+            gu.assert_same_bits(gather(unit["exp_avg_sq"][r], j), ov, "exp_avg_sq u%d r%d" % (u, r))
+            gu.assert_same_bits(gather(unit["full_out"][g], i), obf, "full u%d g%d" % (u, r))
+
+
+def test_llama_block_all_ranks(ora):
+    torch = gu.torch()
+    wl = wls.LLAMA_BLOCK
+    units, info, keep = bench.build_all_ranks(wl, wl.world_size, torch, fs, synth)
+    fs.fsdp_shard_step_grouped(units, 0, wl.world_size, gu.adam_hyper(1))
+    torch.cuda.synchronize()
+    check_all_ranks_unit(ora, wl, 0, units[0], wl.world_size, None, 1, seed=1)
+    del units, keep
+
+
+def test_gpt2_small_grouped(ora):
+    torch = gu.torch()
+    wl = wls.GPT2_SMALL
+    units, info, keep = bench.build_all_ranks(wl, wl.world_size, torch, fs, synth)
+    assert info["params"] == 124439808
+    assert fs.fsdp_shard_step_grouped_launches(units, 0, 8) == 1
+    fs.fsdp_shard_step_grouped(units, 0, wl.world_size, gu.adam_hyper(1))
+    torch.cuda.synchronize()
+    for u in (0, 5, 11, 12):
+        check_all_ranks_unit(ora, wl, u, units[u], wl.world_size, None, 1, seed=10 + u)
+    del units, keep
+
+
+def test_hybrid_full_size_identical_across_F(ora):
+    torch = gu.torch()
+    wl = wls.HYBRID
+    ref_master = ref_full = None
+    for F in (16, 4, 1):
+        units, info, keep = bench.build_all_ranks(wl, F, torch, fs, synth)
+        fs.fsdp_shard_step_grouped(units, 0, wl.world_size, gu.adam_hyper(1))
+        torch.cuda.synchronize()
+        grads, st, full = keep[0]
+        R = wl.world_size // F
+        if ref_master is None:
+            ref_master, ref_full = st[0][0].clone(), full[0].clone()
+            check_all_ranks_unit(ora, wl, 0, units[0], F, None, 1, seed=20)
+        for g in range(R):
+            assert torch.equal(st[0][g].view(torch.int32), ref_master.view(torch.int32)), "F=%d g=%d" % (F, g)
+            assert torch.equal(full[g], ref_full), "full F=%d g=%d" % (F, g)
+        if F == 4:
+            check_all_ranks_unit(ora, wl, 0, units[0], F, None, 1, seed=21)
+        del units, keep, grads, st, full
+        torch.cuda.empty_cache()
+
+
+def test_llama7b_local_rank(ora):
+    """The benchmark's headline workload and launch: one grouped launch over 33 units, rank 0."""
+    torch = gu.torch()
+    wl = wls.LLAMA7B
+    rank = 0
+    units, info, bufs = bench.build_local_rank(wl, rank, torch, fs, synth)
+    assert info["params"] == 6738415616 and info["shard_elems"] == 842301952
+    assert fs.fsdp_shard_step_grouped_launches(units, rank, rank + 1) == 1
+    fs.fsdp_shard_step_grouped(units, rank, rank + 1, gu.adam_hyper(1))
+    torch.cuda.synchronize()
+    W = wl.world_size
+    for u in (0, 1, 17, 31, 32):
+        unit = units[u]
+        lay = unit["layout"]
+        S, P = lay.shard_numel, lay.numel
+        j = sample_positions(S, seed=100 + u)
+        i = rank * S + j
+        rows = [synth.normal_bf16_at(wls.key_grad(wl, u % 2, k, 0), i, wl.sigma_grad) for k in range(W)]
+        master = synth.normal_f32_at(wls.key_master(wl, u), i, wl.sigma_master, n_valid=P)
+        m = synth.normal_f32_at(wls.key_exp_avg(wl, u), i, wl.sigma_state, absval=True, n_valid=P)
+        v = synth.normal_f32_at(wls.key_exp_avg_sq(wl, u), i, wl.sigma_state, absval=True, n_valid=P)
+        op, om, ov, obf = oracle_at(ora, rows, master, m, v, 1)
+        gu.assert_same_bits(gather(unit["master"][0], j), op, "master u%d" % u)
+        gu.assert_same_bits(gather(unit["exp_avg"][0], j), om, "exp_avg u%d" % u)
+        gu.assert_same_bits(gather(unit["exp_avg_sq"][0], j), ov, "exp_avg_sq u%d" % u)
+        gu.assert_same_bits(gather(unit["full_out"][0], i), obf, "own slice u%d" % u)
+        # gathered slices of the other ranks: copies of their shards
+        for k in (1, W - 1):
+            jk = sample_positions(S, k=64, seed=200 + u + k)
+            want = synth.normal_bf16_at(wls.key_shard(wl, u), k * S + jk, wl.sigma_master, n_valid=P)
+            gu.assert_same_bits(gather(unit["full_out"][0], k * S + jk), want, "gathered u%d k%d" % (u, k))
+    del units, bufs
+    torch.cuda.empty_cache()
