@@ -338,7 +338,10 @@ def run_ours(args):
             "mode": info["mode"],
             "parallelism": "W=%d virtual ranks in one GPU's HBM; %d GPU process(es), each an independent "
                            "step, no data-path collective" % (info["W"], nproc),
-            "l2": "inputs larger than L2: %.1f GB touched per step vs 129 MB L2" % (bytes_step / 1e9),
+            "l2": ("inputs larger than L2: %.1f GB touched per step vs 129 MB L2" % (bytes_step / 1e9)
+                   if bytes_step > 2 * 129e6 else
+                   "working set %.0f MB is within 2x the 129 MB L2: L2-resident, not an HBM figure"
+                   % (bytes_step / 1e6)),
             "storage": "bf16 gradients/params, fp32 master/m/v",
         },
         "params_per_s": round(info["elems_per_step"] * nproc / (ms_per_step * 1e-3), 1),

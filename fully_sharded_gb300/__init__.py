@@ -77,7 +77,8 @@ class FsdpError(RuntimeError):
 
 
 def library_path() -> str:
-    return _build_mod.SO
+    """The in-tree library, or the file named by FSDP_GB300_LIB (an alternative build)."""
+    return os.environ.get("FSDP_GB300_LIB") or _build_mod.SO
 
 
 def _load():
