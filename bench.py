@@ -45,6 +45,27 @@ def env_rank():
         int(os.environ.get("LOCAL_RANK", "0"))
 
 
+def virtual_rank(rank: int, world_size_virtual: int) -> int:
+    """The virtual FSDP rank a GPU process steps: independent partitions, one per process."""
+    return rank % world_size_virtual
+
+
+def max_over_ranks(x: float, dist) -> float:
+    """Slowest rank's time (no-op without a process group)."""
+    if dist is None or not dist.is_initialized() or dist.get_world_size() == 1:
+        return x
+    import torch
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_gbs(bytes_per_step_per_rank: int, nproc: int, ms_per_step: float) -> float:
+    """Aggregate algorithmic GB/s: every rank's bytes over the slowest rank's step time."""
+    return bytes_per_step_per_rank * nproc / (ms_per_step * 1e-3) / 1e9
+
+
 def measured_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -246,7 +267,7 @@ def run_ours(args):
         if args.units:
             wl = wls.Workload(wl.name, wl.config_id, wl.units[:args.units], wl.world_size,
                               sigma_state=wl.sigma_state)
-        vrank = rank % wl.world_size
+        vrank = virtual_rank(rank, wl.world_size)
         units, info, bufs = build_local_rank(wl, vrank, torch, fs, synth)
         rb, re = vrank, vrank + 1
         workload_name = "llama7b_local_rank" + ("_units%d" % args.units if args.units else "")
@@ -301,16 +322,12 @@ def run_ours(args):
     clk = clocks.stop()
     if dist:
         dist.barrier()
-    total_ms = start.elapsed_time(stop)
+    total_ms = max_over_ranks(start.elapsed_time(stop), dist)
     launch_ms = [a.elapsed_time(b) for a, b in evs]
-    if dist:
-        tt = torch.tensor([total_ms], device="cuda")
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        total_ms = float(tt.item())
     ms_per_step = total_ms / args.steps
     nproc = world
     bytes_step = info["bytes_per_step"]
-    value = bytes_step * nproc / (ms_per_step * 1e-3) / 1e9
+    value = whole_job_gbs(bytes_step, nproc, ms_per_step)
     peak, peak_kind = measured_peaks()
     mean_launch_ms = statistics.mean(launch_ms) / launches_per_step
     achieved = bytes_step / launches_per_step / (mean_launch_ms * 1e-3) / 1e9
@@ -435,12 +452,8 @@ def e2e_local_rank(args, torch, fs, synth, wl, units, info, bufs, rank, stream, 
         one_step(t)
         t += 1
     torch.cuda.synchronize()
-    ms = (time.perf_counter() - t0) * 1e3 / k
-    if dist:
-        tt = torch.tensor([ms], device="cuda")
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        ms = float(tt.item())
-    return {"value": round(info["bytes_per_step"] * nproc / (ms * 1e-3) / 1e9, 2), "unit": UNIT,
+    ms = max_over_ranks((time.perf_counter() - t0) * 1e3 / k, dist)
+    return {"value": round(whole_job_gbs(info["bytes_per_step"], nproc, ms), 2), "unit": UNIT,
             "h2d_bytes_per_step": h2d_bytes, "d2h_bytes_per_step": d2h_bytes, "ms_per_step": round(ms, 3),
             "steps": k, "note": "host wall clock around K steps, pinned buffers, per-unit calls"}
 
