@@ -69,6 +69,7 @@ int grid_capacity(int variant, int* err) {
       *err = FSDP_ECUDA;
       return 0;
     }
+    if (variant != 5 && per_sm > kBlocksPerSm) per_sm = kBlocksPerSm;
     g_blocks_per_sm[dev][variant].store(per_sm, std::memory_order_relaxed);
   }
   return sms * per_sm;

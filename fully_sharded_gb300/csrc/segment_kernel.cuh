@@ -11,12 +11,13 @@
 //   kCopy    byte copy (all-gather of bf16 shards, pack, unpack; "The forward
 //            cycle: all-gather, compute, reshard")
 //   kZero    zero fill (FlatParameter padding)
-// A segment is cut into fixed-size chunks; chunk c of the whole launch is
-// processed by block c mod gridDim, so all resident blocks stream through the
-// same region of HBM together. The path is HBM-bound (no dense contraction,
-// ~10 fp32 operations per 42+ bytes), so the design goals are 16-byte
-// coalesced accesses, W independent gradient loads in flight per thread, and
-// streaming cache hints; no tensor cores.
+// A segment is cut into fixed-size chunks (2048 elements, or 16 KB for
+// copies); chunk c of the whole launch is processed by block c mod gridDim, so
+// all resident blocks stream through the same region of HBM together. The
+// grid is persistent: kBlocksPerSm blocks on every SM. The path is HBM-bound
+// (no dense contraction, ~10 fp32 operations per 42+ bytes), so the design
+// goals are 16-byte coalesced accesses, many independent loads in flight per
+// thread, and streaming cache hints; no tensor cores.
 //
 // Arithmetic is bit-identical to the definition: fp32 left fold of the W bf16
 // gradients in rank order starting from +0, IEEE division by W (a multiply by
@@ -34,7 +35,12 @@ namespace fsdp {
 constexpr int kThreads = 256;
 constexpr int kVec = 8;                                 // elements per thread per chunk
 constexpr int64_t kChunkElems = int64_t(kThreads) * kVec;  // 2048 elements
-constexpr int64_t kChunkBytes = int64_t(kThreads) * 16;    // 4096 bytes (copy / zero)
+constexpr int kCopyVecs = 4;                              // 16-byte vectors per thread per copy chunk
+constexpr int64_t kChunkBytes = int64_t(kThreads) * 16 * kCopyVecs;  // 16 KB (copy / zero)
+// Resident blocks per SM. Measured on GB300: 3 blocks of 256 threads stream
+// closer to the HBM peak than 4 (W = 2..8: +3..9 %), and replica-heavy hybrid
+// steps at W = 16 gain from 3 over the 2 their register use would allow.
+constexpr int kBlocksPerSm = 3;
 
 enum SegKind : int32_t { kStep = 0, kReduce = 1, kAdam = 2, kCopy = 3, kZero = 4 };
 
@@ -141,19 +147,25 @@ __device__ __forceinline__ void add_bf16x8(float (&acc)[8], const uint4& r) {
   acc[7] = __fadd_rn(acc[7], bf16_hi(r.w));
 }
 
-// Reduced gradient of 8 consecutive elements at e: every row loaded first (W
-// independent 16-byte loads in flight), then folded in rank order.
+// Reduced gradient of 8 consecutive elements at e: the rows of a batch (up to
+// 8) are all loaded first (independent 16-byte loads in flight), then folded
+// in rank order.
 template <int W>
 __device__ __forceinline__ void fold8(const Params& p, const Seg& d, int64_t e, float (&g)[8]) {
 #pragma unroll
   for (int i = 0; i < 8; ++i) g[i] = 0.0f;
   if constexpr (W > 0) {
-    uint4 r[W];
+    // rows in batches of at most 8 (rank order kept) to bound register use
+    constexpr int kBatch = W < 8 ? W : 8;
 #pragma unroll
-    for (int k = 0; k < W; ++k)
-      r[k] = ld_stream_u4(static_cast<const uint16_t*>(p.ptr[d.ptr + k]) + e);
+    for (int k0 = 0; k0 < W; k0 += kBatch) {
+      uint4 r[kBatch];
 #pragma unroll
-    for (int k = 0; k < W; ++k) add_bf16x8(g, r[k]);
+      for (int k = 0; k < kBatch; ++k)
+        r[k] = ld_stream_u4(static_cast<const uint16_t*>(p.ptr[d.ptr + k0 + k]) + e);
+#pragma unroll
+      for (int k = 0; k < kBatch; ++k) add_bf16x8(g, r[k]);
+    }
   } else {
     const int w = p.s.w;
     for (int k0 = 0; k0 < w; k0 += 8) {
@@ -335,12 +347,21 @@ __device__ __forceinline__ void bytes_chunk(const Params& p, const Seg& d, int64
   const int64_t end = (b0 + kChunkBytes < d.n) ? b0 + kChunkBytes : d.n;
   switch (d.width) {
     case 16: {
-      const int64_t b = b0 + int64_t(threadIdx.x) * 16;
-      if (b + 16 <= end) {
-        const uint4 v = kZeroFill ? make_uint4(0, 0, 0, 0) : ld_stream_u4(src + b);
-        st_stream_u4(dst + b, v);
-      } else {
-        for (int64_t i = b; i < end; ++i) dst[i] = kZeroFill ? 0 : src[i];
+      // all loads of the chunk first (64 bytes in flight per thread), then the stores
+      uint4 v[kCopyVecs];
+#pragma unroll
+      for (int k = 0; k < kCopyVecs; ++k) {
+        const int64_t b = b0 + (int64_t(k) * kThreads + threadIdx.x) * 16;
+        if (!kZeroFill && b + 16 <= end) v[k] = ld_stream_u4(src + b);
+      }
+#pragma unroll
+      for (int k = 0; k < kCopyVecs; ++k) {
+        const int64_t b = b0 + (int64_t(k) * kThreads + threadIdx.x) * 16;
+        if (b + 16 <= end) {
+          st_stream_u4(dst + b, kZeroFill ? make_uint4(0, 0, 0, 0) : v[k]);
+        } else {
+          for (int64_t i = b; i < end; ++i) dst[i] = kZeroFill ? 0 : src[i];
+        }
       }
       break;
     }
@@ -368,7 +389,8 @@ __device__ __forceinline__ void bytes_chunk(const Params& p, const Seg& d, int64
 // -------------------------------------------------------------- the kernel
 
 template <int W>
-__global__ void __launch_bounds__(kThreads) segment_kernel(const __grid_constant__ Params p) {
+__global__ void __launch_bounds__(kThreads, (W > 0 ? kBlocksPerSm : 2))
+    segment_kernel(const __grid_constant__ Params p) {
   int s = 0;
   int64_t first = 0;  // first chunk of segment s
   for (int64_t c = blockIdx.x; c < p.total_chunks; c += gridDim.x) {
