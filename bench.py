@@ -34,7 +34,8 @@ if ROOT not in sys.path:
 
 METRIC = "fused FSDP shard-step HBM GB/s and params/s, % of GB300 HBM peak"
 UNIT = "GB/s"
-KERNEL_SOURCES = ["fully_sharded_gb300/csrc/segment_kernel.cuh", "fully_sharded_gb300/csrc/abi.cu"]
+KERNEL_SOURCES = ["fully_sharded_gb300/csrc/segment_kernel.cuh", "fully_sharded_gb300/csrc/abi.cu",
+                  "fully_sharded_gb300/csrc/host_internal.h"]
 TRAFFIC_PROFILE = os.path.join(ROOT, "profiles", "segment_kernel_llama7b_local_rank.md")
 
 
@@ -388,74 +389,102 @@ def run_ours(args):
         print(json.dumps(line), flush=True)
 
 
-def e2e_local_rank(args, torch, fs, synth, wl, units, info, bufs, rank, stream, nproc, dist):
-    """Same metric through the public API with host buffers.
-
-    Per step: host->device copy (pinned memory) of the step's inputs, i.e. the
-    rank's slice of each of the W gradients of every unit, then the per-unit
-    fsdp_shard_step calls, then device->host read of the step's result, the
-    rank's updated bf16 shard of every unit. A second stream copies unit u+1's
-    gradients while unit u computes; the two-slot gradient pool bounds that
-    prefetch to one unit (the transient budget with prefetch = 1)."""
+def pipeline_setup(torch, fs, units, info, rank, n_slots):
+    """Pinned host gradient slices of every unit (W x S each, unit-major), pinned result
+    buffers and a staging pool of n_slots slots, for fsdp_pipeline_step."""
     W = info["W"]
     lays = [u["layout"] for u in units]
     S_tot = info["shard_elems"]
-    # pinned host copies of the inputs each step consumes: W slices of S per unit
-    host_g = torch.empty((W, S_tot), dtype=torch.int16, pin_memory=True)
+    host_g = torch.empty(W * S_tot, dtype=torch.int16, pin_memory=True)
+    host_out = torch.empty(S_tot, dtype=torch.int16, pin_memory=True)
+    punits = []
     so = 0
     for u, lay in enumerate(lays):
         S = lay.shard_numel
+        g = host_g[W * so:W * (so + S)]
         for k in range(W):
-            host_g[k, so:so + S].copy_(units[u]["grads"][k][rank * S:(rank + 1) * S])
+            g[k * S:(k + 1) * S].copy_(units[u]["grads"][k][rank * S:(rank + 1) * S])
+        punits.append(dict(layout=lay, grad_slices=g, master=units[u]["master"][0],
+                           exp_avg=units[u]["exp_avg"][0], exp_avg_sq=units[u]["exp_avg_sq"][0],
+                           other_shards=units[u]["other_shards"], full_out=units[u]["full_out"][0],
+                           shard_out=host_out[so:so + S]))
         so += S
-    host_out = torch.empty(S_tot, dtype=torch.int16, pin_memory=True)
-    copy_stream = torch.cuda.Stream()
-    done = [torch.cuda.Event() for _ in range(2)]  # slot free again
-    ready = [torch.cuda.Event() for _ in range(len(lays))]
-    h2d_bytes = 2 * W * S_tot
-    d2h_bytes = 2 * S_tot
+    slot = max(l.padded_numel for l in lays)
+    staging = torch.empty(n_slots * slot, dtype=torch.int16, device="cuda")
+    return fs.PipelineBatch(punits), staging, slot, (host_g, host_out)
 
-    def one_step(t):
-        so = 0
-        offs = []
-        for u, lay in enumerate(lays):
-            offs.append(so)
-            so += lay.shard_numel
-        for u, lay in enumerate(lays):
-            S = lay.shard_numel
-            slot = u % 2
-            with torch.cuda.stream(copy_stream):
-                copy_stream.wait_event(done[slot])  # the unit that last used this slot is done
-                for k in range(W):
-                    units[u]["grads"][k][rank * S:(rank + 1) * S].copy_(
-                        host_g[k, offs[u]:offs[u] + S], non_blocking=True)
-                copy_stream.record_event(ready[u])
-            stream.wait_event(ready[u])
-            fs.fsdp_shard_step(units[u]["grads"], lay, rank, rank + 1, units[u]["master"],
-                               units[u]["exp_avg"], units[u]["exp_avg_sq"], units[u]["other_shards"],
-                               units[u]["full_out"], fs.AdamHyper(step=t), stream=stream)
-            stream.record_event(done[slot])
-            with torch.cuda.stream(stream):
-                host_out[offs[u]:offs[u] + S].copy_(
-                    units[u]["full_out"][0][rank * S:(rank + 1) * S], non_blocking=True)
 
+def time_pipeline(torch, fs, batch, staging, slot, n_slots, rank, steps, warmup, dist, compute, copy):
     t = 10_000
-    for _ in range(max(1, args.warmup)):
-        one_step(t)
+    for _ in range(max(1, warmup)):
+        fs.fsdp_pipeline_step(batch, rank, staging, slot, n_slots, fs.AdamHyper(step=t), compute=compute,
+                              copy=copy)
         t += 1
     torch.cuda.synchronize()
-    k = max(1, min(args.steps, args.e2e_steps))
     if dist:
         dist.barrier()
     t0 = time.perf_counter()
-    for _ in range(k):
-        one_step(t)
+    for _ in range(steps):
+        fs.fsdp_pipeline_step(batch, rank, staging, slot, n_slots, fs.AdamHyper(step=t), compute=compute,
+                              copy=copy)
         t += 1
     torch.cuda.synchronize()
-    ms = max_over_ranks((time.perf_counter() - t0) * 1e3 / k, dist)
+    return max_over_ranks((time.perf_counter() - t0) * 1e3 / steps, dist)
+
+
+def e2e_local_rank(args, torch, fs, synth, wl, units, info, bufs, rank, stream, nproc, dist):
+    """Same metric through the public API with host buffers.
+
+    Per step, fsdp_pipeline_step copies each unit's inputs (the rank's slice of
+    each of the W gradients) from pinned host memory into a staging slot,
+    steps the unit, and reads the step's result (the rank's new bf16 shard)
+    back to pinned host memory. Two slots: unit u+1's copy overlaps unit u's
+    step (prefetch 1)."""
+    W = info["W"]
+    S_tot = info["shard_elems"]
+    batch, staging, slot, keep = pipeline_setup(torch, fs, units, info, rank, 2)
+    k = max(1, min(args.steps, args.e2e_steps))
+    ms = time_pipeline(torch, fs, batch, staging, slot, 2, rank, k, args.warmup, dist, stream,
+                       torch.cuda.Stream())
     return {"value": round(whole_job_gbs(info["bytes_per_step"], nproc, ms), 2), "unit": UNIT,
-            "h2d_bytes_per_step": h2d_bytes, "d2h_bytes_per_step": d2h_bytes, "ms_per_step": round(ms, 3),
-            "steps": k, "note": "host wall clock around K steps, pinned buffers, per-unit calls"}
+            "h2d_bytes_per_step": 2 * W * S_tot, "d2h_bytes_per_step": 2 * S_tot, "ms_per_step": round(ms, 3),
+            "steps": k, "note": "host wall clock around K fsdp_pipeline_step calls (2 staging slots), "
+                                "pinned host buffers"}
+
+
+def run_pipeline(args):
+    """Prefetch depth 0 / 1 / 2 of fsdp_pipeline_step on the 7B local-rank workload: step
+    time with the inputs arriving from pinned host memory, and the staging pool's bytes
+    against the accountant's transient term 2 U (1 + prefetch)."""
+    import torch
+    import fully_sharded_gb300 as fs
+    import synth
+    from synth import workloads as wls
+    rank, world, local_rank = env_rank()
+    torch.cuda.set_device(local_rank)
+    wl = wls.LLAMA7B
+    vrank = virtual_rank(rank, wl.world_size)
+    units, info, bufs = build_local_rank(wl, vrank, torch, fs, synth)
+    compute, copy = torch.cuda.Stream(), torch.cuda.Stream()
+    res = {}
+    U = max(u["layout"].padded_numel for u in units)
+    for n_slots in (1, 2, 3):
+        batch, staging, slot, keep = pipeline_setup(torch, fs, units, info, vrank, n_slots)
+        ms = time_pipeline(torch, fs, batch, staging, slot, n_slots, vrank, args.steps, args.warmup, None,
+                           compute, copy)
+        acc = fs.fsdp_account(info["params"], U, wl.world_size, wl.world_size, n_slots - 1)
+        res["prefetch_%d" % (n_slots - 1)] = {
+            "ms_per_step": round(ms, 3), "GB_per_s": round(info["bytes_per_step"] / (ms * 1e-3) / 1e9, 2),
+            "staging_bytes": staging.numel() * 2, "accountant_transient_bytes": acc["transient_bytes"]}
+        del batch, staging, keep
+        torch.cuda.empty_cache()
+    base = res["prefetch_0"]["ms_per_step"]
+    print(json.dumps({"workload": "llama7b_local_rank_pipeline", "W": wl.world_size, "rank": vrank,
+                      "units": info["units"], "largest_unit_params": U,
+                      "h2d_bytes_per_step": 2 * wl.world_size * info["shard_elems"],
+                      "results": res,
+                      "speedup_prefetch_1": round(base / res["prefetch_1"]["ms_per_step"], 3),
+                      "speedup_prefetch_2": round(base / res["prefetch_2"]["ms_per_step"], 3)}), flush=True)
 
 
 # -------------------------------------------------------- CPU oracle (baseline)
@@ -578,6 +607,8 @@ def main():
         raise SystemExit("at least 3 warm-up steps")
     if args.impl == "reference":
         run_reference(args)
+    elif args.workload == "pipeline":
+        run_pipeline(args)
     else:
         run_ours(args)
 

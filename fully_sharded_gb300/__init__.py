@@ -23,7 +23,7 @@ __all__ = [
     "fsdp_flatten_layout", "fsdp_pack_flat", "fsdp_unpack_flat", "fsdp_reduce_scatter",
     "fsdp_adam_shard_step", "fsdp_all_gather", "fsdp_shard_step", "fsdp_shard_step_grouped",
     "fsdp_account", "fsdp_status_string", "UnitArgs", "UnitBatch",
-    "fsdp_shard_step_grouped_launches",
+    "fsdp_shard_step_grouped_launches", "fsdp_pipeline_step", "PipelineUnit", "PipelineBatch",
 ]
 
 FSDP_OK = 0
@@ -59,6 +59,12 @@ class UnitArgs(ctypes.Structure):
     _fields_ = [("layout", ctypes.POINTER(Layout)), ("grads", _c_p), ("master", _c_p),
                 ("exp_avg", _c_p), ("exp_avg_sq", _c_p), ("other_shards", _c_p),
                 ("full_out", _c_p)]
+
+
+class PipelineUnit(ctypes.Structure):
+    _fields_ = [("layout", ctypes.POINTER(Layout)), ("grad_slices", _c_p), ("master", _c_p),
+                ("exp_avg", _c_p), ("exp_avg_sq", _c_p), ("other_shards", _c_p), ("full_out", _c_p),
+                ("shard_out", _c_p)]
 
 
 class Account(ctypes.Structure):
@@ -102,6 +108,8 @@ def _load():
         "fsdp_shard_step_grouped_launches": [ctypes.POINTER(UnitArgs), _c_i32, _c_i32, _c_i32,
                                              ctypes.POINTER(_c_i32)],
         "fsdp_account": [_c_dbl, _c_dbl, _c_i32, _c_i32, _c_i32, ctypes.POINTER(Account)],
+        "fsdp_pipeline_step": [ctypes.POINTER(PipelineUnit), _c_i32, _c_i32, P, _c_i64, _c_i32,
+                               ctypes.POINTER(AdamHyper), P, P],
     }
     for name, args in sigs.items():
         fn = getattr(lib, name)
@@ -263,6 +271,48 @@ def fsdp_shard_step_grouped_launches(units, rank_begin: int, rank_end: int) -> i
     _check("fsdp_shard_step_grouped_launches", _lib.fsdp_shard_step_grouped_launches(
         batch.array, batch.n, rank_begin, rank_end, ctypes.byref(n)))
     return n.value
+
+
+def _addr(x) -> int | None:
+    """Address of a tensor in device or (pinned) host memory, or an int address."""
+    if x is None or isinstance(x, int):
+        return x
+    if not x.is_contiguous():
+        raise ValueError("expected a contiguous tensor")
+    return x.data_ptr()
+
+
+class PipelineBatch:
+    """Marshalled units for fsdp_pipeline_step (kept alive together)."""
+
+    def __init__(self, units):
+        self._keep = []
+        self.array = (PipelineUnit * max(1, len(units)))()
+        self.n = len(units)
+        for i, u in enumerate(units):
+            lay = u["layout"]
+            oth = _parray(u["other_shards"], 2)
+            self._keep.append((lay, oth))
+            a = self.array[i]
+            a.layout = ctypes.pointer(lay)
+            a.grad_slices = _addr(u["grad_slices"])
+            a.master = _dptr(u["master"], 4)
+            a.exp_avg = _dptr(u["exp_avg"], 4)
+            a.exp_avg_sq = _dptr(u["exp_avg_sq"], 4)
+            a.other_shards = ctypes.cast(oth, _c_p)
+            a.full_out = _dptr(u["full_out"], 2)
+            a.shard_out = _addr(u.get("shard_out"))
+
+
+def fsdp_pipeline_step(units, rank: int, staging, slot_numel: int, n_slots: int, adam: AdamHyper,
+                       compute=None, copy=None):
+    """Pipelined step of one rank over many units (prefetch = n_slots - 1). `units`: list of
+    dicts (layout, grad_slices, master, exp_avg, exp_avg_sq, other_shards, full_out,
+    shard_out) or a PipelineBatch; `staging`: device bf16 buffer of n_slots * slot_numel."""
+    batch = units if isinstance(units, PipelineBatch) else PipelineBatch(units)
+    _check("fsdp_pipeline_step", _lib.fsdp_pipeline_step(
+        batch.array, batch.n, rank, _dptr(staging, 2), slot_numel, n_slots, ctypes.byref(adam),
+        _stream(compute), _stream(copy)))
 
 
 def fsdp_account(P: float, U: float, N: int, F: int | None = None, prefetch: int = 1) -> dict:

@@ -1,0 +1,117 @@
+// Host-side internals shared by the translation units of the C ABI: the
+// segment list an entry point builds, the overlap check it runs, and the
+// launcher of fsdp::segment_kernel. Not part of the public interface.
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstdint>
+#include <vector>
+
+#include "fsdp.h"
+#include "segment_kernel.cuh"
+
+namespace fsdp {
+
+// ------------------------------------------------------------ segment table
+
+struct SegmentList {
+  std::vector<Seg> seg;
+  std::vector<const void*> ptr;
+
+  static bool aligned16(const void* q) { return (reinterpret_cast<uintptr_t>(q) & 15u) == 0; }
+
+  // kStep / kReduce / kAdam: `ptrs` in pool order; width 16 iff all are aligned.
+  void add_elementwise(SegKind kind, int64_t n, int nrep, const std::vector<const void*>& ptrs) {
+    if (n <= 0) return;
+    bool ok = true;
+    for (const void* q : ptrs) ok = ok && (q == nullptr || aligned16(q));
+    Seg d{};
+    d.n = n;
+    d.kind = kind;
+    d.nrep = nrep;
+    d.ptr = static_cast<int32_t>(ptr.size());
+    d.width = ok ? 16 : 0;
+    seg.push_back(d);
+    ptr.insert(ptr.end(), ptrs.begin(), ptrs.end());
+  }
+
+  void add_bytes(SegKind kind, const void* src, void* dst, int64_t bytes) {
+    if (bytes <= 0) return;
+    const uintptr_t a = reinterpret_cast<uintptr_t>(dst) | (src ? reinterpret_cast<uintptr_t>(src) : 0);
+    int width = 1;
+    if ((a & 15u) == 0) {
+      width = 16;  // a ragged tail is copied byte by byte
+    } else {
+      const uintptr_t b = a | static_cast<uintptr_t>(bytes);
+      width = (b & 7u) == 0 ? 8 : (b & 3u) == 0 ? 4 : (b & 1u) == 0 ? 2 : 1;
+    }
+    Seg d{};
+    d.n = bytes;
+    d.kind = kind;
+    d.ptr = static_cast<int32_t>(ptr.size());
+    d.width = width;
+    seg.push_back(d);
+    if (kind == kCopy) ptr.push_back(src);
+    ptr.push_back(dst);
+  }
+
+  int pool_size(size_t i) const {
+    const int32_t end = (i + 1 < seg.size()) ? seg[i + 1].ptr : static_cast<int32_t>(ptr.size());
+    return end - seg[i].ptr;
+  }
+};
+
+
+// Byte ranges for overlap checks.
+struct Range {
+  uintptr_t lo, hi;
+};
+
+inline Range range_of(const void* p, int64_t bytes) {
+  const uintptr_t a = reinterpret_cast<uintptr_t>(p);
+  return Range{a, a + static_cast<uintptr_t>(bytes)};
+}
+
+class AliasCheck {
+ public:
+  void output(const void* p, int64_t bytes) {
+    if (bytes > 0) out_.push_back(range_of(p, bytes));
+  }
+  void input(const void* p, int64_t bytes) {
+    if (bytes > 0) in_.push_back(range_of(p, bytes));
+  }
+  // True when outputs are pairwise disjoint and no input overlaps an output.
+  bool ok() {
+    std::sort(out_.begin(), out_.end(), [](const Range& a, const Range& b) { return a.lo < b.lo; });
+    for (size_t i = 1; i < out_.size(); ++i)
+      if (out_[i].lo < out_[i - 1].hi) return false;
+    for (const Range& r : in_) {
+      // first output whose end lies beyond r.lo (outputs are disjoint, so ends are sorted too)
+      auto it = std::upper_bound(out_.begin(), out_.end(), r.lo,
+                                 [](uintptr_t v, const Range& o) { return v < o.hi; });
+      if (it != out_.end() && it->lo < r.hi) return false;
+    }
+    return true;
+  }
+
+ private:
+  std::vector<Range> out_, in_;
+};
+
+
+// Launch the list, splitting it where a descriptor table would overflow. With
+// `count` set, nothing is launched and the number of launches is returned there.
+int launch(const SegmentList& list, const Scalars& s, cudaStream_t stream, int* count = nullptr);
+
+// Layout consistent with its own definition (padding, shard length, W, F).
+bool layout_ok(const fsdp_layout_t* L);
+
+// Per-launch fp32 scalars from the Adam hyper-parameters (EINVAL on bad values).
+int make_scalars(const fsdp_adam_t* h, int w, Scalars* s);
+
+// Scalars for launches without Adam (reduce-scatter, copies).
+Scalars reduce_only_scalars(int w);
+
+}  // namespace fsdp

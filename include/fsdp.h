@@ -197,6 +197,48 @@ int fsdp_shard_step_grouped_launches(const fsdp_unit_args_t *units, int32_t n_un
                                      int32_t rank_begin, int32_t rank_end,
                                      int32_t *launches_out);
 
+/* Pipelined step of one rank over many units (full sharding, F = W), with a
+ * bounded pool of staging slots for the incoming gradients.
+ * [notes] "Key results" (backward prefetching: issue the next unit's
+ * collective before the current one finishes), [math] "Overlap: prefetching to
+ * hide the collectives" and "Per-unit memory and communication, in numbers"
+ * (transient = 2 U (1 + prefetch) bytes of bf16 per rank).
+ * For unit u in order, slot s = u mod n_slots:
+ *   on `copy`:    wait until the unit that last used slot s has been stepped,
+ *                 then copy its W x S gradient slices into slot s;
+ *   on `compute`: wait for that copy, run the fused local-rank step of `rank`
+ *                 reading the gradients from slot s (reduce-scatter, Adam,
+ *                 bf16 cast, all-gather of the other shards into full_out),
+ *                 then copy the new bf16 shard to shard_out if given.
+ * With n_slots = 1 (prefetch 0) copies and steps alternate; with n_slots = 2
+ * (prefetch 1) the copy of unit u+1 overlaps the step of unit u.
+ * staging: device bf16 buffer of n_slots x slot_numel elements, caller-owned,
+ * slot_numel >= padded_numel of every unit (its W x S slices); n_slots in
+ * [1, 8]; its contents are overwritten. The pool's size is the transient
+ * gradient budget: 2 * n_slots * slot_numel bytes.
+ * When the call returns, `copy` is ordered after every operation it queued on
+ * `compute`, so later work on either stream sees the results. The two streams
+ * may be the same stream (no overlap). Results are bit-identical to
+ * fsdp_shard_step_grouped on the same values. EINVAL: F != W, a unit with
+ * another W, bad rank, n_slots outside [1,8], a slot too small, null pointers;
+ * EALIAS: outputs overlapping inputs, the staging pool or each other. */
+typedef struct {
+  const fsdp_layout_t *layout;
+  const uint16_t *grad_slices;         /* W x S bf16 (row k = rank k's gradient at the
+                                          owned slice), host (pinned) or device memory */
+  float *master;                       /* device fp32 [S] of the owned rank, in place */
+  float *exp_avg;                      /* device fp32 [S] */
+  float *exp_avg_sq;                   /* device fp32 [S] */
+  const uint16_t *const *other_shards; /* W device pointers by rank; the owned rank's entry
+                                          is ignored */
+  uint16_t *full_out;                  /* device bf16 [padded_numel] */
+  uint16_t *shard_out;                 /* bf16 [S] (host or device) or NULL */
+} fsdp_pipeline_unit_t;
+
+int fsdp_pipeline_step(const fsdp_pipeline_unit_t *units, int32_t n_units, int32_t rank,
+                       uint16_t *staging, int64_t slot_numel, int32_t n_slots,
+                       const fsdp_adam_t *adam, fsdp_stream_t compute, fsdp_stream_t copy);
+
 /* a9. Closed-form accountant (host only).
  * [math] "Why FSDP exists": ~16 bytes per parameter (bf16 weight + bf16 grad +
  * fp32 master + two fp32 Adam moments); DDP keeps 16P on every GPU.

@@ -225,3 +225,28 @@ def test_grouped_rejects_mixed_layouts():
     a, b = u(l4, 0), u(l4, 1)
     b["full_out"] = [a["full_out"][0] + 64]  # two units writing the same full buffer
     _expect(fs.FSDP_EALIAS, fs.fsdp_shard_step_grouped, [a, b], 0, 4, HP)
+
+
+def test_pipeline_rejects_bad_arguments():
+    W, S = 4, 256
+    lay = _lay(W * S, W)
+    unit = dict(layout=lay, grad_slices=_addr(1), master=_addr(2), exp_avg=_addr(3), exp_avg_sq=_addr(4),
+                other_shards=[_addr(5 + k) for k in range(W)], full_out=_addr(10), shard_out=None)
+
+    def call(status, units=None, rank=0, staging=_addr(20), slot=W * S, n_slots=2, adam=HP):
+        with pytest.raises(FsdpError) as e:
+            fs.fsdp_pipeline_step([unit] if units is None else units, rank, staging, slot, n_slots, adam,
+                                  compute=0, copy=0)
+        assert e.value.status == status
+
+    call(fs.FSDP_EINVAL, n_slots=0)
+    call(fs.FSDP_EINVAL, n_slots=9)
+    call(fs.FSDP_EINVAL, slot=W * S - 1)
+    call(fs.FSDP_EINVAL, rank=W)
+    hybrid = dict(unit, layout=_lay(W * S, W, 2))
+    call(fs.FSDP_EINVAL, units=[hybrid])
+    call(fs.FSDP_EINVAL, units=[dict(unit, master=None)])
+    call(fs.FSDP_EINVAL, units=[dict(unit, other_shards=[_addr(5), None, _addr(7), _addr(8)])])
+    call(fs.FSDP_EALIAS, staging=_addr(2))                       # pool overlaps the master shard
+    call(fs.FSDP_EALIAS, units=[dict(unit, shard_out=_addr(10) + 64)])
+    call(fs.FSDP_EALIAS, units=[unit, dict(unit, grad_slices=_addr(30))])  # two units, same outputs
