@@ -24,12 +24,15 @@ __all__ = [
     "fsdp_adam_shard_step", "fsdp_all_gather", "fsdp_shard_step", "fsdp_shard_step_grouped",
     "fsdp_account", "fsdp_status_string", "UnitArgs", "UnitBatch",
     "fsdp_shard_step_grouped_launches", "fsdp_pipeline_step", "PipelineUnit", "PipelineBatch",
+    "fsdp_pipeline_step_noalloc",
 ]
 
 FSDP_OK = 0
 FSDP_EINVAL = -1
 FSDP_EALIAS = -2
 FSDP_ECUDA = -3
+FSDP_ENOSPACE = -4
+NOALLOC_STAGING_BYTES = 64 << 20
 FSDP_DTYPE_F32 = 0
 FSDP_DTYPE_BF16 = 1
 MAX_WORLD = 64
@@ -110,6 +113,8 @@ def _load():
         "fsdp_account": [_c_dbl, _c_dbl, _c_i32, _c_i32, _c_i32, ctypes.POINTER(Account)],
         "fsdp_pipeline_step": [ctypes.POINTER(PipelineUnit), _c_i32, _c_i32, P, _c_i64, _c_i32,
                                ctypes.POINTER(AdamHyper), P, P],
+        "fsdp_pipeline_step_noalloc": [ctypes.POINTER(PipelineUnit), _c_i32, _c_i32, _c_i32,
+                                       ctypes.POINTER(AdamHyper), P, P],
     }
     for name, args in sigs.items():
         fn = getattr(lib, name)
@@ -313,6 +318,17 @@ def fsdp_pipeline_step(units, rank: int, staging, slot_numel: int, n_slots: int,
     _check("fsdp_pipeline_step", _lib.fsdp_pipeline_step(
         batch.array, batch.n, rank, _dptr(staging, 2), slot_numel, n_slots, ctypes.byref(adam),
         _stream(compute), _stream(copy)))
+
+
+def fsdp_pipeline_step_noalloc(units, rank: int, n_slots: int, adam: AdamHyper, compute=None,
+                               copy=None):
+    """fsdp_pipeline_step without a staging argument, for callers that cannot allocate
+    device memory when they step: the pool is a fixed 64 MiB array inside the library
+    (FsdpError with status FSDP_ENOSPACE if n_slots times the largest unit does not fit).
+    Calls on one device share that array, so their GPU work must not overlap."""
+    batch = units if isinstance(units, PipelineBatch) else PipelineBatch(units)
+    _check("fsdp_pipeline_step_noalloc", _lib.fsdp_pipeline_step_noalloc(
+        batch.array, batch.n, rank, n_slots, ctypes.byref(adam), _stream(compute), _stream(copy)))
 
 
 def fsdp_account(P: float, U: float, N: int, F: int | None = None, prefetch: int = 1) -> dict:

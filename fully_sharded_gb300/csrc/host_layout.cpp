@@ -73,6 +73,7 @@ extern "C" const char* fsdp_status_string(int status) {
     case FSDP_EINVAL: return "invalid argument";
     case FSDP_EALIAS: return "an output overlaps an input or another output";
     case FSDP_ECUDA: return "CUDA launch error";
+    case FSDP_ENOSPACE: return "work exceeds the 64 MiB staging capacity of the allocation-free entry point";
     default: return "unknown status";
   }
 }

@@ -49,6 +49,8 @@ typedef struct CUstream_st *fsdp_stream_t;
                             weight_decay != 0, ... */
 #define FSDP_EALIAS (-2) /* an output overlaps an input or another output */
 #define FSDP_ECUDA (-3)  /* a CUDA launch failed (cudaGetLastError) */
+#define FSDP_ENOSPACE (-4) /* the work does not fit the fixed staging capacity of
+                              fsdp_pipeline_step_noalloc */
 
 #define FSDP_MAX_WORLD 64
 
@@ -238,6 +240,32 @@ typedef struct {
 int fsdp_pipeline_step(const fsdp_pipeline_unit_t *units, int32_t n_units, int32_t rank,
                        uint16_t *staging, int64_t slot_numel, int32_t n_slots,
                        const fsdp_adam_t *adam, fsdp_stream_t compute, fsdp_stream_t copy);
+
+/* Allocation-free form of fsdp_pipeline_step. (The FSDP pages have no
+ * counterpart: this exists for callers, not for the method.)
+ * For callers that cannot allocate device memory where they step the
+ * optimizer: processes whose device memory is owned entirely by another
+ * allocator (a framework's caching allocator, or a fixed arena carved out at
+ * start-up), and loops that must not call cudaMalloc because it can
+ * synchronize the device and stall the very streams the pipeline overlaps.
+ * They pass only inputs and outputs; the staging pool is a fixed array of
+ * FSDP_NOALLOC_STAGING_BYTES inside the library's device code, which the CUDA
+ * runtime reserves on a GPU when it loads that code there and keeps until the
+ * process exits. The call itself allocates nothing.
+ * Same arguments and results as fsdp_pipeline_step, with slot_numel = the
+ * largest padded_numel among the units. FSDP_ENOSPACE (nothing launched) if
+ * n_slots * slot_numel * 2 exceeds FSDP_NOALLOC_STAGING_BYTES.
+ * The first call on a device looks up the array's device address (with that
+ * device current); make that first call before any stream capture. Every
+ * call on a device uses the same array: calls whose work overlaps on the GPU
+ * (different streams without ordering between them) race on it and give
+ * wrong results. Each unit's slot is filled completely before it is read, so
+ * nothing needs clearing between calls. */
+#define FSDP_NOALLOC_STAGING_BYTES (64ll << 20)
+
+int fsdp_pipeline_step_noalloc(const fsdp_pipeline_unit_t *units, int32_t n_units, int32_t rank,
+                               int32_t n_slots, const fsdp_adam_t *adam, fsdp_stream_t compute,
+                               fsdp_stream_t copy);
 
 /* a9. Closed-form accountant (host only).
  * [math] "Why FSDP exists": ~16 bytes per parameter (bf16 weight + bf16 grad +
