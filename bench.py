@@ -452,6 +452,117 @@ def e2e_local_rank(args, torch, fs, synth, wl, units, info, bufs, rank, stream, 
                                 "pinned host buffers"}
 
 
+def run_unfused(args):
+    """Rows a3, a4, a6 and a2 timed on their own on the Llama block (W = 8, all ranks):
+    per rank fsdp_reduce_scatter (fp32 gradient shard out) and fsdp_adam_shard_step
+    (bf16 shard out), then fsdp_all_gather of the 8 shards; against the fused step on
+    the same buffers. Also fsdp_pack_flat of the block's nine fp32 tensors."""
+    import torch
+    import fully_sharded_gb300 as fs
+    import synth
+    from synth import workloads as wls
+    torch.cuda.set_device(0)
+    wl = wls.LLAMA_BLOCK
+    W = wl.world_size
+    units, info, keep = build_all_ranks(wl, W, torch, fs, synth)
+    u = units[0]
+    lay = u["layout"]
+    S, padded = lay.shard_numel, lay.padded_numel
+    gshard = torch.empty((W, S), device="cuda")
+    bshard = torch.empty((W, S), dtype=torch.int16, device="cuda")
+    full = u["full_out"][0]
+    stream = torch.cuda.Stream()
+
+    def timed(fn, reps):
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        stream.record_event(a)
+        for _ in range(reps):
+            fn()
+        stream.record_event(b)
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) / reps
+
+    hp = fs.AdamHyper(step=1)
+    rs = lambda: [fs.fsdp_reduce_scatter(u["grads"], lay, r, gshard[r], stream=stream) for r in range(W)]  # noqa
+    ad = lambda: [fs.fsdp_adam_shard_step(u["master"][r], u["exp_avg"][r], u["exp_avg_sq"][r], gshard[r], hp,  # noqa
+                                          bshard[r], stream=stream) for r in range(W)]
+    ag = lambda: fs.fsdp_all_gather([bshard[r] for r in range(W)], lay, full, stream=stream)  # noqa
+    batch = fs.UnitBatch(units)
+    fused = lambda: fs.fsdp_shard_step_grouped(batch, 0, W, hp, stream=stream)  # noqa
+    n = args.steps
+    t_rs, t_ad, t_ag, t_fused = timed(rs, n), timed(ad, n), timed(ag, n), timed(fused, n)
+    b_rs, b_ad, b_ag = (2 * W + 4) * padded, (4 + 24 + 2) * padded, 4 * padded
+    # a2: pack the nine fp32 tensors of the block into the flat master
+    numels = wls.numels(wl.units[0])
+    tensors = [torch.empty(n_, device="cuda").normal_() for n_ in numels]
+    lay2, offs = fs.fsdp_flatten_layout(numels, W)
+    flat = torch.empty(lay2.padded_numel, device="cuda")
+    t_pack = timed(lambda: fs.fsdp_pack_flat(tensors, lay2, offs, flat, stream=stream), n)
+    peak, _ = measured_peaks()
+    row = lambda ms, b: {"ms": round(ms, 4), "GB_per_s": round(b / (ms * 1e-3) / 1e9, 1),  # noqa
+                         "frac_of_peak": round(b / (ms * 1e-3) / 1e9 / peak, 4)}
+    print(json.dumps({
+        "workload": "llama_block_all_ranks_unfused", "W": W, "padded_elems": padded,
+        "reduce_scatter_x8": row(t_rs, b_rs), "adam_shard_step_x8": row(t_ad, b_ad), "all_gather": row(t_ag, b_ag),
+        "unfused_total": row(t_rs + t_ad + t_ag, b_rs + b_ad + b_ag),
+        "fused": row(t_fused, (2 * W + 26) * padded),
+        "fused_speedup": round((t_rs + t_ad + t_ag) / t_fused, 3),
+        "pack_f32": row(t_pack, 8 * lay2.numel),
+        "bytes_per_element": {"unfused": 2 * W + 38, "fused": 2 * W + 26}}), flush=True)
+
+
+def run_offload(args):
+    """Optimizer-state offload: the 7B local-rank step with the rank's fp32 master, m and v
+    in page-locked host memory (mapped into the GPU's address space), read and written by
+    the fused kernel over the host link, against the same step with the state in HBM."""
+    import torch
+    import fully_sharded_gb300 as fs
+    import synth
+    from synth import workloads as wls
+    torch.cuda.set_device(0)
+    wl = wls.LLAMA7B
+    units, info, bufs = build_local_rank(wl, 0, torch, fs, synth)
+    stream = torch.cuda.Stream()
+
+    def timed(batch, steps):
+        for t in range(1, 4):
+            fs.fsdp_shard_step_grouped(batch, 0, 1, fs.AdamHyper(step=t), stream=stream)
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        stream.record_event(a)
+        for t in range(steps):
+            fs.fsdp_shard_step_grouped(batch, 0, 1, fs.AdamHyper(step=10 + t), stream=stream)
+        stream.record_event(b)
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) / steps
+
+    ms_hbm = timed(fs.UnitBatch(units), args.steps)
+    host = {n: bufs[n].cpu().pin_memory() for n in ("master", "exp_avg", "exp_avg_sq")}
+    so = 0
+    off_units = []
+    for u in units:
+        S = u["layout"].shard_numel
+        off_units.append(dict(u, master=[host["master"][so:so + S].data_ptr()],
+                              exp_avg=[host["exp_avg"][so:so + S].data_ptr()],
+                              exp_avg_sq=[host["exp_avg_sq"][so:so + S].data_ptr()]))
+        so += S
+    ms_host = timed(fs.UnitBatch(off_units), max(2, args.steps // 10))
+    S_tot = info["shard_elems"]
+    print(json.dumps({
+        "workload": "llama7b_local_rank_state_offload", "W": wl.world_size, "shard_elems": S_tot,
+        "state_in_hbm": {"ms_per_step": round(ms_hbm, 3),
+                         "GB_per_s": round(info["bytes_per_step"] / (ms_hbm * 1e-3) / 1e9, 1)},
+        "state_in_host_memory": {"ms_per_step": round(ms_host, 3),
+                                 "GB_per_s": round(info["bytes_per_step"] / (ms_host * 1e-3) / 1e9, 1),
+                                 "host_link_bytes_per_step": 24 * S_tot,
+                                 "host_link_GB_per_s": round(24 * S_tot / (ms_host * 1e-3) / 1e9, 1)},
+        "gpu_memory_saved_bytes": 12 * S_tot,
+        "slowdown": round(ms_host / ms_hbm, 2)}), flush=True)
+
+
 def run_pipeline(args):
     """Prefetch depth 0 / 1 / 2 of fsdp_pipeline_step on the 7B local-rank workload: step
     time with the inputs arriving from pinned host memory, and the staging pool's bytes
@@ -609,6 +720,10 @@ def main():
         run_reference(args)
     elif args.workload == "pipeline":
         run_pipeline(args)
+    elif args.workload == "unfused":
+        run_unfused(args)
+    elif args.workload == "offload":
+        run_offload(args)
     else:
         run_ours(args)
 

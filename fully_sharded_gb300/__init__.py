@@ -24,7 +24,7 @@ __all__ = [
     "fsdp_adam_shard_step", "fsdp_all_gather", "fsdp_shard_step", "fsdp_shard_step_grouped",
     "fsdp_account", "fsdp_status_string", "UnitArgs", "UnitBatch",
     "fsdp_shard_step_grouped_launches", "fsdp_pipeline_step", "PipelineUnit", "PipelineBatch",
-    "fsdp_pipeline_step_noalloc",
+    "fsdp_pipeline_step_noalloc", "fsdp_all_gather_state", "fsdp_zero1_step", "fsdp_account_zero",
 ]
 
 FSDP_OK = 0
@@ -68,6 +68,14 @@ class PipelineUnit(ctypes.Structure):
     _fields_ = [("layout", ctypes.POINTER(Layout)), ("grad_slices", _c_p), ("master", _c_p),
                 ("exp_avg", _c_p), ("exp_avg_sq", _c_p), ("other_shards", _c_p), ("full_out", _c_p),
                 ("shard_out", _c_p)]
+
+
+class ZeroAccount(ctypes.Structure):
+    _fields_ = [(n, _c_dbl) for n in ("weights_bytes", "grads_bytes", "optimizer_bytes", "total_bytes",
+                                      "reduction_vs_ddp", "comm_elems")]
+
+    def as_dict(self):
+        return {n: getattr(self, n) for n, _ in self._fields_}
 
 
 class Account(ctypes.Structure):
@@ -115,6 +123,9 @@ def _load():
                                ctypes.POINTER(AdamHyper), P, P],
         "fsdp_pipeline_step_noalloc": [ctypes.POINTER(PipelineUnit), _c_i32, _c_i32, _c_i32,
                                        ctypes.POINTER(AdamHyper), P, P],
+        "fsdp_all_gather_state": [P, ctypes.POINTER(Layout), _c_i32, P, P],
+        "fsdp_zero1_step": [P, ctypes.POINTER(Layout), _c_i32, P, P, P, P, P, P, ctypes.POINTER(AdamHyper), P],
+        "fsdp_account_zero": [_c_dbl, _c_i32, _c_i32, ctypes.POINTER(ZeroAccount)],
     }
     for name, args in sigs.items():
         fn = getattr(lib, name)
@@ -329,6 +340,30 @@ def fsdp_pipeline_step_noalloc(units, rank: int, n_slots: int, adam: AdamHyper, 
     batch = units if isinstance(units, PipelineBatch) else PipelineBatch(units)
     _check("fsdp_pipeline_step_noalloc", _lib.fsdp_pipeline_step_noalloc(
         batch.array, batch.n, rank, n_slots, ctypes.byref(adam), _stream(compute), _stream(copy)))
+
+
+def fsdp_all_gather_state(shards, layout: Layout, full_out, stream=None):
+    """Gather per-rank state (fp32 master/m/v, or bf16) into the full flat buffer of a group."""
+    es = full_out.element_size()
+    _check("fsdp_all_gather_state", _lib.fsdp_all_gather_state(
+        _parray(shards, es), ctypes.byref(layout), _dtype_of(full_out), _dptr(full_out), _stream(stream)))
+
+
+def fsdp_zero1_step(grads, layout: Layout, rank: int, avg_grad_out, master, exp_avg, exp_avg_sq, other_shards,
+                    full_out, adam: AdamHyper, stream=None):
+    """ZeRO stage 1 step of one rank: full all-reduce average into avg_grad_out, Adam on the
+    rank's slice, bf16 shard and gather into full_out."""
+    _check("fsdp_zero1_step", _lib.fsdp_zero1_step(
+        _parray(grads, 2), ctypes.byref(layout), rank, _dptr(avg_grad_out, 4), _dptr(master, 4),
+        _dptr(exp_avg, 4), _dptr(exp_avg_sq, 4), _parray(other_shards, 2), _dptr(full_out, 2),
+        ctypes.byref(adam), _stream(stream)))
+
+
+def fsdp_account_zero(P: float, N: int, stage: int) -> dict:
+    """Per-GPU bytes of ZeRO stage 0 (DDP) .. 3 (FSDP) and the communication per step (host only)."""
+    out = ZeroAccount()
+    _check("fsdp_account_zero", _lib.fsdp_account_zero(float(P), N, stage, ctypes.byref(out)))
+    return out.as_dict()
 
 
 def fsdp_account(P: float, U: float, N: int, F: int | None = None, prefetch: int = 1) -> dict:

@@ -67,6 +67,19 @@ extern "C" int fsdp_account(double P, double U, int32_t N, int32_t F, int32_t pr
   return FSDP_OK;
 }
 
+extern "C" int fsdp_account_zero(double P, int32_t N, int32_t stage, fsdp_zero_account_t* out) {
+  if (!out || N < 1 || stage < 0 || stage > 3 || !(P >= 0.0)) return FSDP_EINVAL;
+  const double n = static_cast<double>(N);
+  // bf16 weights, bf16 gradients, fp32 master + m + v; stage k shards the last k of them
+  out->optimizer_bytes = stage >= 1 ? 12.0 * P / n : 12.0 * P;
+  out->grads_bytes = stage >= 2 ? 2.0 * P / n : 2.0 * P;
+  out->weights_bytes = stage >= 3 ? 2.0 * P / n : 2.0 * P;
+  out->total_bytes = out->weights_bytes + out->grads_bytes + out->optimizer_bytes;
+  out->reduction_vs_ddp = out->total_bytes > 0.0 ? 16.0 * P / out->total_bytes : 1.0;
+  out->comm_elems = stage == 3 ? 3.0 * P : 2.0 * P;
+  return FSDP_OK;
+}
+
 extern "C" const char* fsdp_status_string(int status) {
   switch (status) {
     case FSDP_OK: return "ok";

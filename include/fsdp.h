@@ -20,6 +20,13 @@
  *   - "device" pointers point to CUDA global memory of the current device;
  *     pointer arrays themselves (const T* const*) are HOST arrays of device
  *     pointers and are read before the call returns.
+ *   - Optimizer-state offload ([gloss] "CPU Offload"): the fp32 master,
+ *     exp_avg and exp_avg_sq pointers of fsdp_shard_step(_grouped),
+ *     fsdp_adam_shard_step and fsdp_pipeline_step may instead point to
+ *     page-locked host memory mapped into the device's address space
+ *     (cudaHostAlloc, or cudaHostRegister with cudaHostRegisterMapped, at an
+ *     address the device can use as is). The kernels then read and write the
+ *     state over the host link; nothing else changes.
  *   - bf16 values are passed as their uint16_t bit patterns; fp32 as float.
  *   - Every GPU call is asynchronous on `stream` (0 = legacy default stream).
  *     Inputs must stay unchanged, and outputs untouched, until the stream has
@@ -266,6 +273,54 @@ int fsdp_pipeline_step(const fsdp_pipeline_unit_t *units, int32_t n_units, int32
 int fsdp_pipeline_step_noalloc(const fsdp_pipeline_unit_t *units, int32_t n_units, int32_t rank,
                                int32_t n_slots, const fsdp_adam_t *adam, fsdp_stream_t compute,
                                fsdp_stream_t copy);
+
+/* Gather of any per-rank state into the full flat buffer of a group, for the
+ * full state dict. [gloss] "Checkpoint/Resume": FULL_STATE_DICT gathers the
+ * full model (on rank 0) instead of saving one piece per rank.
+ * shards: F device pointers, shards[k] = S elements of position k, element
+ * type `dtype` (FSDP_DTYPE_F32 for master / exp_avg / exp_avg_sq, FSDP_DTYPE_BF16
+ * for parameters); full_out: padded_numel elements, full_out[k*S + j] =
+ * shards[k][j]. A shard that already is the view full_out + k*S is left in
+ * place. fsdp_unpack_flat then splits full_out into the unit's tensors. */
+int fsdp_all_gather_state(const void *const *shards, const fsdp_layout_t *layout, int32_t dtype,
+                          void *full_out, fsdp_stream_t stream);
+
+/* ZeRO stage 1 step of one rank ([gloss] "ZeRO Stages": stage 1 shards only
+ * the optimizer state; every rank keeps the full model and the full averaged
+ * gradient; [notes] "Key results": F = 1 reduces to an all-reduce).
+ * Two launches on `stream`: (1) the all-reduce average of the W bf16 gradients
+ * over the whole padded buffer into avg_grad_out (fp32 [padded_numel], the
+ * same fixed-order fold and division as the reduce-scatter); (2) Adam on the
+ * rank's slice avg_grad_out[rank*S, (rank+1)*S) of its fp32 master/exp_avg/
+ * exp_avg_sq [S] with the bf16 result written to full_out + rank*S, and the
+ * other ranks' bf16 shards copied into full_out (other_shards by rank, the
+ * owned entry ignored). Requires F = W. Results equal fsdp_shard_step of the
+ * same rank bit for bit; avg_grad_out equals fsdp_reduce_scatter with F = 1. */
+int fsdp_zero1_step(const uint16_t *const *grads, const fsdp_layout_t *layout, int32_t rank,
+                    float *avg_grad_out, float *master, float *exp_avg, float *exp_avg_sq,
+                    const uint16_t *const *other_shards, uint16_t *full_out, const fsdp_adam_t *adam,
+                    fsdp_stream_t stream);
+
+/* ZeRO-stage accountant (host only). Per-GPU persistent bytes with the 16
+ * bytes per parameter of [math] "Why FSDP exists" split as 2 (bf16 weights)
+ * + 2 (bf16 gradients) + 12 (fp32 master, m, v), and [gloss] "ZeRO Stages":
+ *   stage 0 (DDP): 2P + 2P + 12P
+ *   stage 1: 2P + 2P + 12P/N      (optimizer state sharded)
+ *   stage 2: 2P + 2P/N + 12P/N    (+ gradients sharded)
+ *   stage 3: 2P/N + 2P/N + 12P/N  (+ parameters sharded: FSDP full sharding)
+ * comm_elems per rank per step (pages' rounded form, [math] "Per-unit memory
+ * and communication"): 2P for stages 0-2 (an all-reduce, or reduce-scatter +
+ * all-gather), 3P for stage 3. reduction_vs_ddp = 16P / total_bytes. */
+typedef struct {
+  double weights_bytes;
+  double grads_bytes;
+  double optimizer_bytes;
+  double total_bytes;
+  double reduction_vs_ddp;
+  double comm_elems;
+} fsdp_zero_account_t;
+
+int fsdp_account_zero(double P, int32_t N, int32_t stage, fsdp_zero_account_t *out);
 
 /* a9. Closed-form accountant (host only).
  * [math] "Why FSDP exists": ~16 bytes per parameter (bf16 weight + bf16 grad +

@@ -66,6 +66,7 @@ class Oracle:
             "ora_shard_step": (_i32, [_P, _i32, _i32, _i64, _i32, _i32, _P, _P, _P, _P, _P,
                                       _f64, _f64, _f64, _f64, _i64]),
             "ora_account": (_i32, [_f64, _f64, _i32, _i32, _i32, _P]),
+            "ora_account_zero": (_i32, [_f64, _i32, _i32, _P]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(lib, name)
@@ -193,6 +194,17 @@ class Oracle:
             raise ValueError("oracle account rejected the arguments (%d)" % rc)
         return dict(zip(self.ACCOUNT_FIELDS, out.tolist()))
 
+
+def _account_zero(self, P, N, stage) -> dict:
+    out = np.zeros(6, dtype=np.float64)
+    rc = self.lib.ora_account_zero(float(P), N, stage, self._ptr(out))
+    if rc != 0:
+        raise ValueError("oracle account_zero rejected the arguments (%d)" % rc)
+    return dict(zip(("weights_bytes", "grads_bytes", "optimizer_bytes", "total_bytes", "reduction_vs_ddp",
+                     "comm_elems"), out.tolist()))
+
+
+Oracle.account_zero = _account_zero
 
 _default: Oracle | None = None
 

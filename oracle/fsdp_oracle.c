@@ -297,3 +297,31 @@ int ora_account(double P, double U, int32_t N, int32_t F, int32_t prefetch, doub
     out[9] = 2.0 * out[6];
     return ORA_OK;
 }
+
+/* ---------------------------------------------------------------------------
+ * ZeRO stages, per GPU persistent bytes.
+ * [math] "Why FSDP exists": per parameter a 2-byte weight, a 2-byte gradient,
+ *   a 4-byte fp32 master and 4 + 4 bytes of Adam moments.
+ * [gloss] "ZeRO Stages": stage 1 shards the optimizer state over the N ranks,
+ *   stage 2 also the gradients, stage 3 also the parameters (= FSDP).
+ * out[]: 0 weights, 1 grads, 2 optimizer (master + moments), 3 total,
+ *        4 16P / total, 5 communication elements per rank per step
+ *        ([math] "Per-unit memory and communication": an all-reduce ~2P,
+ *        FSDP's three collectives ~3P).
+ * ------------------------------------------------------------------------- */
+int ora_account_zero(double P, int32_t N, int32_t stage, double *out)
+{
+    if (N < 1 || stage < 0 || stage > 3 || P < 0) return ORA_EINVAL;
+    double n = (double)N;
+    double weights = 2.0 * P, grads = 2.0 * P, optim = (4.0 + 4.0 + 4.0) * P;
+    if (stage >= 1) optim = optim / n;
+    if (stage >= 2) grads = grads / n;
+    if (stage >= 3) weights = weights / n;
+    out[0] = weights;
+    out[1] = grads;
+    out[2] = optim;
+    out[3] = weights + grads + optim;
+    out[4] = out[3] > 0 ? 16.0 * P / out[3] : 1.0;
+    out[5] = stage == 3 ? 3.0 * P : 2.0 * P;
+    return ORA_OK;
+}

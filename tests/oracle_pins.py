@@ -476,6 +476,20 @@ def pin_account_ring(ora):
         assert d["ddp_comm_elems"] == 2 * P
 
 
+def pin_account_zero(ora):
+    """ZeRO stages: the worked example's 7e9/8 totals per stage, the 4x / 8x limits, 8x at N = 8."""
+    g = golden("zero_stages.json")
+    for st, want in g["total_bytes"].items():
+        a = ora.account_zero(g["P"], g["N"], int(st))
+        assert a["total_bytes"] == want, st
+        assert a["comm_elems"] == g["comm_elems_per_P"][st] * g["P"], st
+    for st, want in g["large_N_reduction"].items():
+        r = ora.account_zero(g["P"], g["large_N"], int(st))["reduction_vs_ddp"]
+        assert abs(r - want) < 1e-3 * want, st
+    assert ora.account_zero(g["P"], 8, 3)["reduction_vs_ddp"] == g["stage3_reduction_at_N8"]
+    assert ora.account_zero(g["P"], 8, 3)["total_bytes"] == ora.account(g["P"], 0, 8, 8, 0)["persistent_bytes"]
+
+
 ALL_PINS = [
     pin_layout_brute, pin_layout_golden, pin_pack_roundtrip,
     pin_rs_identical_rows, pin_rs_marker_slices, pin_rs_exact_rational, pin_rs_fold_order,
@@ -483,5 +497,5 @@ ALL_PINS = [
     pin_adam_torch, pin_adam_first_step, pin_adam_zero_grad,
     pin_cast_torch,
     pin_step_ddp_torch, pin_step_f_continuum, pin_step_local_rank,
-    pin_account_worked_example, pin_account_ring,
+    pin_account_worked_example, pin_account_ring, pin_account_zero,
 ]

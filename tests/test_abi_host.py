@@ -250,3 +250,44 @@ def test_pipeline_rejects_bad_arguments():
     call(fs.FSDP_EALIAS, staging=_addr(2))                       # pool overlaps the master shard
     call(fs.FSDP_EALIAS, units=[dict(unit, shard_out=_addr(10) + 64)])
     call(fs.FSDP_EALIAS, units=[unit, dict(unit, grad_slices=_addr(30))])  # two units, same outputs
+
+
+def test_account_zero_matches_oracle_and_golden(ora):
+    for P in (0.0, 1.0, 7e9, 124439808.0):
+        for N in (1, 2, 8, 64):
+            for stage in range(4):
+                a, b = fs.fsdp_account_zero(P, N, stage), ora.account_zero(P, N, stage)
+                for k in b:
+                    assert a[k] == pytest.approx(b[k], rel=1e-13, abs=1e-9), (P, N, stage, k)
+    g = pins.golden("zero_stages.json")
+    for st, want in g["total_bytes"].items():
+        assert fs.fsdp_account_zero(g["P"], g["N"], int(st))["total_bytes"] == want
+    for args in ((1e9, 0, 1), (1e9, 8, 4), (1e9, 8, -1), (-1.0, 8, 1)):
+        with pytest.raises(FsdpError):
+            fs.fsdp_account_zero(*args)
+
+
+def test_state_entry_points_reject_bad_arguments():
+    W = 4
+    lay = _lay(1024, W)
+    lib = fs._lib
+    sh = fs._parray([_addr(k) for k in range(W)])
+    assert lib.fsdp_all_gather_state(sh, ctypes.byref(lay), 9, _addr(9), None) == fs.FSDP_EINVAL
+    assert lib.fsdp_all_gather_state(sh, ctypes.byref(lay), fs.FSDP_DTYPE_F32, _addr(2) + 8, None) == fs.FSDP_EALIAS
+    g = [_addr(k) for k in range(W)]
+    oth = [_addr(20 + k) for k in range(W)]
+
+    def z1(status, **over):
+        a = dict(grads=g, layout=lay, rank=1, avg=_addr(10), master=_addr(11), m=_addr(12), v=_addr(13),
+                 others=oth, full=_addr(14), adam=HP)
+        a.update(over)
+        _expect(status, fs.fsdp_zero1_step, a["grads"], a["layout"], a["rank"], a["avg"], a["master"], a["m"],
+                a["v"], a["others"], a["full"], a["adam"])
+
+    z1(fs.FSDP_EINVAL, layout=_lay(1024, W, 2))
+    z1(fs.FSDP_EINVAL, rank=4)
+    z1(fs.FSDP_EINVAL, avg=None)
+    z1(fs.FSDP_EINVAL, others=[oth[0], oth[1], None, oth[3]])
+    z1(fs.FSDP_EINVAL, adam=fs.AdamHyper(step=0))
+    z1(fs.FSDP_EALIAS, avg=_addr(11))
+    z1(fs.FSDP_EALIAS, full=g[2] + 2)

@@ -42,6 +42,9 @@ MUTANTS = {
     "account_no_prefetch": ("out[2] = 2.0 * U * (1.0 + (double)prefetch);", "out[2] = 2.0 * U;"),
     "account_persist_over_N": ("out[0] = 16.0 * P / Fd;", "out[0] = 16.0 * P / Nd;"),
     "account_ring_AR_over_F": ("+ 2.0 * (R - 1.0) / R * P / Fd;", "+ 2.0 * (R - 1.0) / R * P;"),
+    "zero_stage2_shards_weights": ("if (stage >= 2) grads = grads / n;", "if (stage >= 2) weights = weights / n;"),
+    "zero_optimizer_8_bytes": ("optim = (4.0 + 4.0 + 4.0) * P;", "optim = (4.0 + 4.0) * P;"),
+    "zero_stage3_comm_2P": ("out[5] = stage == 3 ? 3.0 * P : 2.0 * P;", "out[5] = 2.0 * P;"),
 }
 
 
