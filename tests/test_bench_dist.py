@@ -53,3 +53,29 @@ def test_two_ranks_take_the_slowest_time_and_aggregate_bytes():
 def test_single_process_is_a_no_op():
     assert bench.max_over_ranks(3.5, None) == 3.5
     assert bench.virtual_rank(9, 8) == 1
+
+
+def _dying_worker(rank, world, port, out):
+    import datetime
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world, timeout=datetime.timedelta(seconds=5))
+    if rank == 1:
+        os._exit(0)  # this rank leaves between steps, before the timing exchange
+    try:
+        bench.max_over_ranks(10.0, dist)
+        out.put((rank, "no error"))
+    except Exception as e:  # the survivor must see the failure on the host, not hang
+        out.put((rank, "error: %s" % type(e).__name__))
+
+
+def test_a_rank_that_leaves_is_detected_by_the_other():
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_dying_worker, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    rank, status = q.get(timeout=120)
+    for p in procs:
+        p.join(timeout=60)
+    assert rank == 0 and status.startswith("error"), status
