@@ -81,10 +81,25 @@ int64_t chunks_of(const Seg& d) {
   return (d.n + unit - 1) / unit;
 }
 
+// Programmatic dependent launch: the launch and block placement of this grid
+// overlap the tail of the previous kernel on the stream (measured on GB300:
+// 1e7-element step 66.3 -> 64.5 us, 7B local-rank step 8.64 -> 8.57 ms); the
+// kernel's griddepcontrol.wait keeps every memory access after the previous
+// kernel has completed.
 template <int W>
 cudaError_t launch_variant(const Params& p, int grid, cudaStream_t stream) {
-  segment_kernel<W><<<grid, kThreads, 0, stream>>>(p);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, segment_kernel<W>, p);
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 }  // namespace

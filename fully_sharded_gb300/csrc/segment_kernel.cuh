@@ -391,6 +391,12 @@ __device__ __forceinline__ void bytes_chunk(const Params& p, const Seg& d, int64
 template <int W>
 __global__ void __launch_bounds__(kThreads, (W > 0 ? kBlocksPerSm : 2))
     segment_kernel(const __grid_constant__ Params p) {
+  // Launched with programmatic stream serialization (see abi.cu): this grid
+  // may be placed on the SMs while the previous kernel of the stream drains.
+  // Wait for that kernel to complete, with its writes visible, before the
+  // first memory access; then allow the next launch to be scheduled early.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;");
   int s = 0;
   int64_t first = 0;  // first chunk of segment s
   for (int64_t c = blockIdx.x; c < p.total_chunks; c += gridDim.x) {
