@@ -561,6 +561,62 @@ def run_offload(args):
         "slowdown": round(ms_host / ms_hbm, 2)}), flush=True)
 
 
+def run_state(args):
+    """NEXT-2 / NEXT-3 rows timed on the Llama block (W = 8): the ZeRO-1 step of rank 0
+    (full all-reduce average kept, then the rank's Adam and gather) against the fused
+    local-rank step on the same buffers, and the full-state gather + unflatten of the
+    fp32 master (8 shards -> flat -> 9 tensors)."""
+    import torch
+    import fully_sharded_gb300 as fs
+    import synth
+    from synth import workloads as wls
+    torch.cuda.set_device(0)
+    wl = wls.Workload("llama_block_local", 2, [wls.LLAMA_BLOCK_UNIT], 8, sigma_state=1e-4)
+    units, info, bufs = build_local_rank(wl, 0, torch, fs, synth)
+    u = units[0]
+    lay = u["layout"]
+    W, S, padded = lay.world_size, lay.shard_numel, lay.padded_numel
+    avg = torch.empty(padded, device="cuda")
+    stream = torch.cuda.Stream()
+
+    def timed(fn, reps):
+        for _ in range(3):
+            fn()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        stream.record_event(a)
+        for _ in range(reps):
+            fn()
+        stream.record_event(b)
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) / reps
+
+    hp = fs.AdamHyper(step=1)
+    batch = fs.UnitBatch(units)
+    t_fused = timed(lambda: fs.fsdp_shard_step_grouped(batch, 0, 1, hp, stream=stream), args.steps)
+    t_zero1 = timed(lambda: fs.fsdp_zero1_step(u["grads"], lay, 0, avg, u["master"][0], u["exp_avg"][0],
+                                               u["exp_avg_sq"][0], u["other_shards"], u["full_out"][0], hp,
+                                               stream=stream), args.steps)
+    b_fused = (6 * W + 22) * S
+    b_zero1 = (2 * W + 4) * padded + (4 + 24 + 2) * S + 4 * (W - 1) * S
+    # full state dict of the fp32 master: gather W shards, unflatten into the 9 tensors
+    shards = [torch.empty(S, device="cuda") for _ in range(W)]
+    flat = torch.empty(padded, device="cuda")
+    numels = wls.numels(wl.units[0])
+    _, offs = fs.fsdp_flatten_layout(numels, W)
+    outs = [torch.empty(n, device="cuda") for n in numels]
+    t_gather = timed(lambda: fs.fsdp_all_gather_state(shards, lay, flat, stream=stream), args.steps)
+    t_unpack = timed(lambda: fs.fsdp_unpack_flat(flat, lay, offs, outs, stream=stream), args.steps)
+    peak, _ = measured_peaks()
+    row = lambda ms, b: {"ms": round(ms, 4), "GB_per_s": round(b / (ms * 1e-3) / 1e9, 1),  # noqa
+                         "frac_of_peak": round(b / (ms * 1e-3) / 1e9 / peak, 4)}
+    print(json.dumps({"workload": "llama_block_rank0_state", "W": W, "shard_elems": S,
+                      "fused_local_step": row(t_fused, b_fused), "zero1_step": row(t_zero1, b_zero1),
+                      "zero1_over_fused_time": round(t_zero1 / t_fused, 3),
+                      "gather_state_f32": row(t_gather, 8 * padded), "unpack_f32": row(t_unpack, 8 * padded)}),
+          flush=True)
+
+
 def run_pipeline(args):
     """Prefetch depth 0 / 1 / 2 of fsdp_pipeline_step on the 7B local-rank workload: step
     time with the inputs arriving from pinned host memory, and the staging pool's bytes
@@ -722,6 +778,8 @@ def main():
         run_unfused(args)
     elif args.workload == "offload":
         run_offload(args)
+    elif args.workload == "state":
+        run_state(args)
     else:
         run_ours(args)
 
