@@ -148,7 +148,7 @@ class ClockSampler:
 
 # --------------------------------------------------------------- workloads
 
-def build_local_rank(wl, rank, torch, fs, synth, hp_step=1):
+def build_local_rank(wl, rank, torch, fs, synth):
     """Device buffers of one rank's step over all units (local-rank mode)."""
     from synth import workloads as wls
     W = wl.world_size

@@ -291,3 +291,13 @@ def test_state_entry_points_reject_bad_arguments():
     z1(fs.FSDP_EINVAL, adam=fs.AdamHyper(step=0))
     z1(fs.FSDP_EALIAS, avg=_addr(11))
     z1(fs.FSDP_EALIAS, full=g[2] + 2)
+
+
+def test_import_fails_loudly_without_the_cuda_library(tmp_path):
+    """No fallback: with the library missing, importing the package raises."""
+    import subprocess
+    import sys
+    env = dict(os.environ, FSDP_GB300_LIB=str(tmp_path / "missing.so"))
+    r = subprocess.run([sys.executable, "-c", "import fully_sharded_gb300"], cwd=ROOT, env=env,
+                       capture_output=True, text=True, timeout=120)
+    assert r.returncode != 0 and "ImportError" in r.stderr
