@@ -16,7 +16,9 @@
  * Conventions for every call:
  *   - The caller owns all memory. The library allocates nothing and keeps no
  *     state about the data between calls (it caches the SM count and kernel
- *     occupancy per device).
+ *     occupancy per device; fsdp_pipeline_step creates and releases CUDA
+ *     events within a call; fsdp_pipeline_step_noalloc stages through a fixed
+ *     array that is part of the library's device code, see there).
  *   - "device" pointers point to CUDA global memory of the current device;
  *     pointer arrays themselves (const T* const*) are HOST arrays of device
  *     pointers and are read before the call returns.
