@@ -35,7 +35,7 @@ if ROOT not in sys.path:
 METRIC = "fused FSDP shard-step HBM GB/s and params/s, % of GB300 HBM peak"
 UNIT = "GB/s"
 KERNEL_SOURCES = ["fully_sharded_gb300/csrc/segment_kernel.cuh", "fully_sharded_gb300/csrc/abi.cu",
-                  "fully_sharded_gb300/csrc/host_internal.h"]
+                  "fully_sharded_gb300/csrc/host_internal.h", "fully_sharded_gb300/csrc/tma_kernel.cuh"]
 TRAFFIC_PROFILE = os.path.join(ROOT, "profiles", "segment_kernel_llama7b_local_rank.md")
 
 

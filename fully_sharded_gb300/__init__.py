@@ -25,6 +25,7 @@ __all__ = [
     "fsdp_account", "fsdp_status_string", "UnitArgs", "UnitBatch",
     "fsdp_shard_step_grouped_launches", "fsdp_pipeline_step", "PipelineUnit", "PipelineBatch",
     "fsdp_pipeline_step_noalloc", "fsdp_all_gather_state", "fsdp_zero1_step", "fsdp_account_zero",
+    "fsdp_shard_step_grouped_plan", "fsdp_device_status", "fsdp_selftest_wait_timeout",
 ]
 
 FSDP_OK = 0
@@ -126,6 +127,10 @@ def _load():
         "fsdp_all_gather_state": [P, ctypes.POINTER(Layout), _c_i32, P, P],
         "fsdp_zero1_step": [P, ctypes.POINTER(Layout), _c_i32, P, P, P, P, P, P, ctypes.POINTER(AdamHyper), P],
         "fsdp_account_zero": [_c_dbl, _c_i32, _c_i32, ctypes.POINTER(ZeroAccount)],
+        "fsdp_shard_step_grouped_plan": [ctypes.POINTER(UnitArgs), _c_i32, _c_i32, _c_i32,
+                                         ctypes.POINTER(_c_i32), ctypes.POINTER(_c_i32)],
+        "fsdp_device_status": [_c_i32, ctypes.POINTER(ctypes.c_uint32)],
+        "fsdp_selftest_wait_timeout": [P, P, _c_i64, _c_i64, P, ctypes.POINTER(ctypes.c_uint32)],
     }
     for name, args in sigs.items():
         fn = getattr(lib, name)
@@ -364,6 +369,31 @@ def fsdp_account_zero(P: float, N: int, stage: int) -> dict:
     out = ZeroAccount()
     _check("fsdp_account_zero", _lib.fsdp_account_zero(float(P), N, stage, ctypes.byref(out)))
     return out.as_dict()
+
+
+def fsdp_shard_step_grouped_plan(units, rank_begin: int, rank_end: int):
+    """Host only: (launches, launches in the TMA form) of fsdp_shard_step_grouped for these units."""
+    batch = units if isinstance(units, UnitBatch) else UnitBatch(units)
+    n, t = _c_i32(0), _c_i32(0)
+    _check("fsdp_shard_step_grouped_plan", _lib.fsdp_shard_step_grouped_plan(
+        batch.array, batch.n, rank_begin, rank_end, ctypes.byref(n), ctypes.byref(t)))
+    return n.value, t.value
+
+
+def fsdp_device_status(clear: bool = False) -> int:
+    """The current device's sticky status word (bit 0: a bounded wait of the TMA form ran out)."""
+    v = ctypes.c_uint32(0)
+    _check("fsdp_device_status", _lib.fsdp_device_status(1 if clear else 0, ctypes.byref(v)))
+    return v.value
+
+
+def fsdp_selftest_wait_timeout(src, dst, wait_limit_ns: int, stream=None) -> int:
+    """Provokes one bounded-wait timeout on a copy of src into dst; returns the status word seen."""
+    v = ctypes.c_uint32(0)
+    nbytes = src.numel() * src.element_size()
+    _check("fsdp_selftest_wait_timeout", _lib.fsdp_selftest_wait_timeout(
+        _dptr(src), _dptr(dst), nbytes, int(wait_limit_ns), _stream(stream), ctypes.byref(v)))
+    return v.value
 
 
 def fsdp_account(P: float, U: float, N: int, F: int | None = None, prefetch: int = 1) -> dict:

@@ -7,6 +7,14 @@
 #include "segment_kernel.cuh"
 #include "host_internal.h"
 
+namespace fsdp {
+// Sticky per-device status word: bit 0 is set when a bounded wait of the TMA
+// form ran out (see tma_kernel.cuh). Read and cleared with fsdp_device_status.
+__device__ unsigned int g_fsdp_status;
+}  // namespace fsdp
+
+#include "tma_kernel.cuh"
+
 #include <algorithm>
 #include <atomic>
 #include <cmath>
@@ -20,7 +28,8 @@ namespace {
 // ------------------------------------------------------------ device facts
 
 constexpr int kMaxDevices = 64;
-constexpr int kNumVariants = 6;  // W = 1, 2, 4, 8, 16, generic
+constexpr int kNumVariants = 7;  // W = 1, 2, 4, 8, 16, generic; 6 = the TMA form (W = 8)
+constexpr int kTmaVariant = 6;
 
 std::atomic<int> g_sm_count[kMaxDevices];
 std::atomic<int> g_blocks_per_sm[kMaxDevices][kNumVariants];
@@ -43,6 +52,7 @@ const void* kernel_of(int variant) {
     case 2: return reinterpret_cast<const void*>(&segment_kernel<4>);
     case 3: return reinterpret_cast<const void*>(&segment_kernel<8>);
     case 4: return reinterpret_cast<const void*>(&segment_kernel<16>);
+    case kTmaVariant: return reinterpret_cast<const void*>(&tma_kernel<8>);
     default: return reinterpret_cast<const void*>(&segment_kernel<0>);
   }
 }
@@ -64,13 +74,20 @@ int grid_capacity(int variant, int* err) {
   }
   int per_sm = g_blocks_per_sm[dev][variant].load(std::memory_order_relaxed);
   if (per_sm == 0) {
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel_of(variant), kThreads, 0) !=
-            cudaSuccess ||
+    const bool tma = variant == kTmaVariant;
+    const int smem = tma ? TmaCfg<8>::kSmemBytes : 0;
+    if (tma && cudaFuncSetAttribute(kernel_of(variant), cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
+                   cudaSuccess) {
+      *err = FSDP_ECUDA;
+      return 0;
+    }
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel_of(variant), tma ? kTmaThreads : kThreads,
+                                                      smem) != cudaSuccess ||
         per_sm <= 0) {
       *err = FSDP_ECUDA;
       return 0;
     }
-    if (variant != 5 && per_sm > kBlocksPerSm) per_sm = kBlocksPerSm;
+    if (variant < 5 && per_sm > kBlocksPerSm) per_sm = kBlocksPerSm;
     g_blocks_per_sm[dev][variant].store(per_sm, std::memory_order_relaxed);
   }
   return sms * per_sm;
@@ -102,15 +119,54 @@ cudaError_t launch_variant(const Params& p, int grid, cudaStream_t stream) {
   return e != cudaSuccess ? e : cudaGetLastError();
 }
 
+cudaError_t launch_tma(const Params& p, int grid, cudaStream_t stream) {
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kTmaThreads);
+  cfg.dynamicSmemBytes = TmaCfg<8>::kSmemBytes;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, tma_kernel<8>, p);
+  return e != cudaSuccess ? e : cudaGetLastError();
+}
+
+// The TMA form pays off for W = 8 launches whose positions each have one
+// replica and that give every block enough chunks to fill its pipeline.
+bool use_tma(const Params& p, int tma_grid) {
+  if (p.s.w != 8) return false;
+  for (int k = 0; k < p.nseg; ++k)
+    if (p.seg[k].kind == kStep && p.seg[k].nrep != 1) return false;
+  return p.total_chunks >= static_cast<int64_t>(kTmaMinChunksPerBlock) * tma_grid;
+}
+
 }  // namespace
 
-int launch(const SegmentList& list, const Scalars& s, cudaStream_t stream, int* count) {
+int launch(const SegmentList& list, const Scalars& s, cudaStream_t stream, int* count, int* tma_count) {
   if (count) *count = 0;
+  if (tma_count) *tma_count = 0;
   if (list.seg.empty()) return FSDP_OK;
   const int variant = variant_of(s.w);
   int err = FSDP_OK;
   const int cap = count ? 1 : grid_capacity(variant, &err);
   if (err != FSDP_OK) return err;
+  // the TMA form's grid: one block per SM (its pipeline fills 224 KB of shared memory)
+  int tma_cap = 0;
+  if (s.w == 8) {
+    if (count) {
+      int dev = 0, sms = 0;
+      tma_cap = (cudaGetDevice(&dev) == cudaSuccess &&
+                 cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess)
+                    ? sms
+                    : 152;
+    } else {
+      tma_cap = grid_capacity(kTmaVariant, &err);
+      if (err != FSDP_OK) return err;
+    }
+  }
   static thread_local Params p;  // ~27 KB: keep it off the stack
   size_t i = 0;
   while (i < list.seg.size()) {
@@ -132,8 +188,17 @@ int launch(const SegmentList& list, const Scalars& s, cudaStream_t stream, int* 
     }
     p.nseg = nseg;
     p.total_chunks = chunks;
+    p.wait_limit_ns = kDefaultWaitLimitNs;
+    p.inject_tx = 0;
+    const bool tma = use_tma(p, tma_cap);
     if (count) {
       ++*count;
+      if (tma && tma_count) ++*tma_count;
+      continue;
+    }
+    if (tma) {
+      if (launch_tma(p, static_cast<int>(std::min<int64_t>(chunks, tma_cap)), stream) != cudaSuccess)
+        return FSDP_ECUDA;
       continue;
     }
     const int grid = static_cast<int>(std::min<int64_t>(chunks, cap));
@@ -257,8 +322,9 @@ using namespace fsdp;
 namespace {
 
 int grouped(const fsdp_unit_args_t* units, int32_t n_units, int32_t rank_begin, int32_t rank_end,
-            const fsdp_adam_t* adam, cudaStream_t stream, int* count) {
+            const fsdp_adam_t* adam, cudaStream_t stream, int* count, int* tma_count = nullptr) {
   if (count) *count = 0;
+  if (tma_count) *tma_count = 0;
   if (n_units < 0 || (n_units > 0 && !units)) return FSDP_EINVAL;
   if (n_units == 0) return FSDP_OK;
   const fsdp_layout_t* L0 = units[0].layout;
@@ -280,7 +346,7 @@ int grouped(const fsdp_unit_args_t* units, int32_t n_units, int32_t rank_begin, 
     if (int rc = build_unit(units[i], rank_begin, rank_end, list, alias)) return rc;
   }
   if (!alias.ok()) return FSDP_EALIAS;
-  return launch(list, s, stream, count);
+  return launch(list, s, stream, count, tma_count);
 }
 
 }  // namespace
@@ -295,11 +361,65 @@ extern "C" int fsdp_shard_step_grouped(const fsdp_unit_args_t* units, int32_t n_
 extern "C" int fsdp_shard_step_grouped_launches(const fsdp_unit_args_t* units, int32_t n_units,
                                                 int32_t rank_begin, int32_t rank_end,
                                                 int32_t* launches_out) {
+  return fsdp_shard_step_grouped_plan(units, n_units, rank_begin, rank_end, launches_out, nullptr);
+}
+
+extern "C" int fsdp_shard_step_grouped_plan(const fsdp_unit_args_t* units, int32_t n_units, int32_t rank_begin,
+                                            int32_t rank_end, int32_t* launches_out, int32_t* tma_launches_out) {
   if (!launches_out) return FSDP_EINVAL;
-  int count = 0;
-  const int rc = grouped(units, n_units, rank_begin, rank_end, nullptr, nullptr, &count);
-  if (rc == FSDP_OK) *launches_out = count;
+  int count = 0, tma = 0;
+  const int rc = grouped(units, n_units, rank_begin, rank_end, nullptr, nullptr, &count, &tma);
+  if (rc == FSDP_OK) {
+    *launches_out = count;
+    if (tma_launches_out) *tma_launches_out = tma;
+  }
   return rc;
+}
+
+extern "C" int fsdp_device_status(int32_t clear, uint32_t* status_out) {
+  if (!status_out) return FSDP_EINVAL;
+  unsigned int v = 0;
+  if (cudaMemcpyFromSymbol(&v, g_fsdp_status, sizeof(v)) != cudaSuccess) return FSDP_ECUDA;
+  if (clear) {
+    const unsigned int z = 0;
+    if (cudaMemcpyToSymbol(g_fsdp_status, &z, sizeof(z)) != cudaSuccess) return FSDP_ECUDA;
+  }
+  *status_out = v;
+  return FSDP_OK;
+}
+
+extern "C" int fsdp_selftest_wait_timeout(const void* src, void* dst, int64_t bytes, int64_t wait_limit_ns,
+                                          fsdp_stream_t stream, uint32_t* status_out) {
+  if (!src || !dst || !status_out || bytes < kChunkBytes || bytes > (int64_t(1) << 30)) return FSDP_EINVAL;
+  if (wait_limit_ns <= 0 || wait_limit_ns > 10000000000ll) return FSDP_EINVAL;
+  if ((reinterpret_cast<uintptr_t>(src) | reinterpret_cast<uintptr_t>(dst)) & 15u) return FSDP_EINVAL;
+  AliasCheck alias;
+  alias.output(dst, bytes);
+  alias.input(src, bytes);
+  if (!alias.ok()) return FSDP_EALIAS;
+  int err = FSDP_OK;
+  const int cap = grid_capacity(kTmaVariant, &err);
+  if (err != FSDP_OK) return err;
+  const unsigned int z = 0;
+  if (cudaMemcpyToSymbol(g_fsdp_status, &z, sizeof(z)) != cudaSuccess) return FSDP_ECUDA;
+  SegmentList list;
+  list.add_bytes(kCopy, src, dst, bytes & ~int64_t(15));
+  static thread_local Params p;
+  std::memset(&p, 0, sizeof(p));
+  p.s = reduce_only_scalars(8);
+  p.nseg = 1;
+  p.seg[0] = list.seg[0];
+  p.seg[0].ptr = 0;
+  p.ptr[0] = list.ptr[0];
+  p.ptr[1] = list.ptr[1];
+  p.total_chunks = (p.seg[0].n + kChunkBytes - 1) / kChunkBytes;
+  p.seg[0].chunk_end = p.total_chunks;
+  p.wait_limit_ns = static_cast<uint64_t>(wait_limit_ns);
+  p.inject_tx = 16;  // block 0's first stage expects 16 bytes that no copy delivers
+  const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  if (launch_tma(p, static_cast<int>(std::min<int64_t>(p.total_chunks, cap)), st) != cudaSuccess) return FSDP_ECUDA;
+  if (cudaStreamSynchronize(st) != cudaSuccess) return FSDP_ECUDA;
+  return fsdp_device_status(1, status_out);
 }
 
 extern "C" int fsdp_shard_step(const uint16_t* const* grads, const fsdp_layout_t* layout,

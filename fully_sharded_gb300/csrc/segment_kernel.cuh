@@ -79,8 +79,9 @@ constexpr int kMaxPtr = 2048;
 struct Params {
   Scalars s;
   int32_t nseg;
-  int32_t reserved;
+  int32_t inject_tx;       // self-test only: extra bytes expected on block 0's first staged chunk
   int64_t total_chunks;
+  uint64_t wait_limit_ns;  // bound of every mbarrier wait in the TMA form
   Seg seg[kMaxSeg];
   const void* ptr[kMaxPtr];
 };

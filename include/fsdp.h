@@ -208,6 +208,32 @@ int fsdp_shard_step_grouped_launches(const fsdp_unit_args_t *units, int32_t n_un
                                      int32_t rank_begin, int32_t rank_end,
                                      int32_t *launches_out);
 
+/* As fsdp_shard_step_grouped_launches, and *tma_launches_out (if not NULL)
+ * receives how many of those launches use the TMA form of the kernel (bulk
+ * copies into a shared-memory pipeline; chosen for W = 8 launches with one
+ * replica per position and enough chunks to fill every SM's pipeline). Needs
+ * no GPU, but reads the SM count of the current device when one is present. */
+int fsdp_shard_step_grouped_plan(const fsdp_unit_args_t *units, int32_t n_units,
+                                 int32_t rank_begin, int32_t rank_end, int32_t *launches_out,
+                                 int32_t *tma_launches_out);
+
+/* The current device's sticky status word (synchronizes the device). Bit 0 is
+ * set when a bounded wait of the TMA form ran out (2 s on one mbarrier): the
+ * block that saw it stopped early, so the outputs of that launch are not
+ * valid. This does not happen in a correct run. clear != 0 resets the word
+ * after reading it. EINVAL: status_out NULL; ECUDA: the read failed. */
+int fsdp_device_status(int32_t clear, uint32_t *status_out);
+
+/* Self-test of the bounded waits: launches the TMA form on a copy of `bytes`
+ * (>= 16384, <= 2^30, both pointers 16-byte aligned, not overlapping) with
+ * block 0's first stage expecting 16 bytes that no copy delivers, and a wait
+ * limit of wait_limit_ns (1 ns .. 10 s). The block gives up after the limit,
+ * drains its copies and returns; the call synchronizes `stream`, then reads
+ * and clears the status word into *status_out (1 when the timeout was seen).
+ * dst is partly written. Nothing hangs and the context stays usable. */
+int fsdp_selftest_wait_timeout(const void *src, void *dst, int64_t bytes, int64_t wait_limit_ns,
+                               fsdp_stream_t stream, uint32_t *status_out);
+
 /* Pipelined step of one rank over many units (full sharding, F = W), with a
  * bounded pool of staging slots for the incoming gradients.
  * [notes] "Key results" (backward prefetching: issue the next unit's
