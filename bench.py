@@ -36,7 +36,7 @@ METRIC = "fused FSDP shard-step HBM GB/s and params/s, % of GB300 HBM peak"
 UNIT = "GB/s"
 KERNEL_SOURCES = ["fully_sharded_gb300/csrc/segment_kernel.cuh", "fully_sharded_gb300/csrc/abi.cu",
                   "fully_sharded_gb300/csrc/host_internal.h", "fully_sharded_gb300/csrc/tma_kernel.cuh"]
-TRAFFIC_PROFILE = os.path.join(ROOT, "profiles", "segment_kernel_llama7b_local_rank.md")
+TRAFFIC_PROFILE = os.path.join(ROOT, "profiles", "tma_kernel_llama7b_local_rank.md")
 
 
 # ------------------------------------------------------------------ helpers
@@ -292,7 +292,7 @@ def run_ours(args):
     else:
         raise SystemExit("unknown workload %s" % name)
     batch = fs.UnitBatch(units)
-    launches_per_step = fs.fsdp_shard_step_grouped_launches(batch, rb, re)
+    launches_per_step, tma_launches = fs.fsdp_shard_step_grouped_plan(batch, rb, re)
     stream = torch.cuda.Stream()
 
     # warm-up
@@ -370,7 +370,8 @@ def run_ours(args):
             "unit": "GB/s",
             "frac": round(achieved / peak, 4),
             "peak_source": peak_kind,
-            "kernel": "fsdp::segment_kernel<%d>" % (info["W"] if info["W"] in (1, 2, 4, 8, 16) else 0),
+            "kernel": ("fsdp::tma_kernel<8>" if tma_launches == launches_per_step else
+                       "fsdp::segment_kernel<%d>" % (info["W"] if info["W"] in (1, 2, 4, 8, 16) else 0)),
             "traffic": traffic,
         },
         "gpu_launches": launches_per_step * args.steps,
