@@ -134,13 +134,24 @@ cudaError_t launch_tma(const Params& p, int grid, cudaStream_t stream) {
   return e != cudaSuccess ? e : cudaGetLastError();
 }
 
-// The TMA form pays off for W = 8 launches whose positions each have one
-// replica and that give every block enough chunks to fill its pipeline.
+// The TMA form pays off for W = 8 step launches whose positions each have one
+// replica and that give every block enough chunks to fill its pipeline. Its
+// producer stages only step and copy chunks; a launch holding any other kind
+// (reduce, Adam, zero fill) or no step at all stays on the LDG form, whose 24
+// warps per SM carry such chunks better than the TMA form's 8 consumers.
 bool use_tma(const Params& p, int tma_grid) {
   if (p.s.w != 8) return false;
-  for (int k = 0; k < p.nseg; ++k)
-    if (p.seg[k].kind == kStep && p.seg[k].nrep != 1) return false;
-  return p.total_chunks >= static_cast<int64_t>(kTmaMinChunksPerBlock) * tma_grid;
+  bool step = false;
+  for (int k = 0; k < p.nseg; ++k) {
+    const Seg& d = p.seg[k];
+    if (d.kind == kStep) {
+      if (d.nrep != 1) return false;
+      step = true;
+    } else if (d.kind != kCopy) {
+      return false;
+    }
+  }
+  return step && p.total_chunks >= static_cast<int64_t>(kTmaMinChunksPerBlock) * tma_grid;
 }
 
 }  // namespace
