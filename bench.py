@@ -443,12 +443,39 @@ def e2e_local_rank(args, torch, fs, synth, wl, units, info, bufs, rank, stream, 
     S_tot = info["shard_elems"]
     batch, staging, slot, keep = pipeline_setup(torch, fs, units, info, rank, 2)
     k = max(1, min(args.steps, args.e2e_steps))
-    ms = time_pipeline(torch, fs, batch, staging, slot, 2, rank, k, args.warmup, dist, stream,
-                       torch.cuda.Stream())
+    copy = torch.cuda.Stream()
+    ms = time_pipeline(torch, fs, batch, staging, slot, 2, rank, k, args.warmup, dist, stream, copy)
+    h2d_bytes = 2 * W * S_tot
+    link = host_link(torch, copy)
+    floor_ms = h2d_bytes / (link["h2d_GB_per_s"] * 1e9) * 1e3
+    link.update({"floor_ms": round(floor_ms, 2), "frac_of_floor": round(floor_ms / ms, 4)})
     return {"value": round(whole_job_gbs(info["bytes_per_step"], nproc, ms), 2), "unit": UNIT,
-            "h2d_bytes_per_step": 2 * W * S_tot, "d2h_bytes_per_step": 2 * S_tot, "ms_per_step": round(ms, 3),
-            "steps": k, "note": "host wall clock around K fsdp_pipeline_step calls (2 staging slots), "
-                                "pinned host buffers"}
+            "h2d_bytes_per_step": h2d_bytes, "d2h_bytes_per_step": 2 * S_tot, "ms_per_step": round(ms, 3),
+            "steps": k, "host_link": link,
+            "note": "host wall clock around K fsdp_pipeline_step calls (2 staging slots), pinned host "
+                    "buffers; host_link: pinned copy bandwidth measured right after, floor_ms = the "
+                    "step's H2D bytes at that rate"}
+
+
+def host_link(torch, stream, nbytes=1 << 31, reps=3):
+    """Pinned host <-> device copy bandwidth (GB/s), best of `reps` single copies of `nbytes`
+    on `stream`: the bound of a step whose inputs arrive from host memory."""
+    host = torch.empty(nbytes // 2, dtype=torch.int16, pin_memory=True)
+    host.zero_()
+    dev = torch.empty(nbytes // 2, dtype=torch.int16, device="cuda")
+    out = {}
+    for name, dst, src in (("h2d_GB_per_s", dev, host), ("d2h_GB_per_s", host, dev)):
+        best = float("inf")
+        for _ in range(reps):
+            torch.cuda.synchronize()
+            t0 = time.perf_counter()
+            with torch.cuda.stream(stream):
+                dst.copy_(src, non_blocking=True)
+            stream.synchronize()
+            best = min(best, time.perf_counter() - t0)
+        out[name] = round(nbytes / best / 1e9, 1)
+    del host, dev
+    return out
 
 
 def run_unfused(args):
@@ -645,7 +672,10 @@ def run_pipeline(args):
         del batch, staging, keep
         torch.cuda.empty_cache()
     base = res["prefetch_0"]["ms_per_step"]
+    link = host_link(torch, copy)
+    link["floor_ms"] = round(2 * wl.world_size * info["shard_elems"] / (link["h2d_GB_per_s"] * 1e9) * 1e3, 2)
     print(json.dumps({"workload": "llama7b_local_rank_pipeline", "W": wl.world_size, "rank": vrank,
+                      "host_link": link,
                       "units": info["units"], "largest_unit_params": U,
                       "h2d_bytes_per_step": 2 * wl.world_size * info["shard_elems"],
                       "results": res,
