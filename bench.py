@@ -326,6 +326,8 @@ def run_ours(args):
     ms_per_step = total_ms / args.steps
     nproc = world
     bytes_step = info["bytes_per_step"]
+    # L2 size as the device reports it (129 MB on GB300 when the property is absent)
+    l2 = float(getattr(torch.cuda.get_device_properties(local_rank), "L2_cache_size", 0) or 129e6)
     value = whole_job_gbs(bytes_step, nproc, ms_per_step)
     peak, peak_kind = measured_peaks()
     mean_launch_ms = local_ms / (args.steps * launches_per_step)  # this rank's launches
@@ -354,10 +356,10 @@ def run_ours(args):
             "mode": info["mode"],
             "parallelism": "W=%d virtual ranks in one GPU's HBM; %d GPU process(es), each an independent "
                            "step, no data-path collective" % (info["W"], nproc),
-            "l2": ("inputs larger than L2: %.1f GB touched per step vs 129 MB L2" % (bytes_step / 1e9)
-                   if bytes_step > 2 * 129e6 else
-                   "working set %.0f MB is within 2x the 129 MB L2: L2-resident, not an HBM figure"
-                   % (bytes_step / 1e6)),
+            "l2": ("inputs larger than L2: %.1f GB touched per step vs %.0f MB L2" % (bytes_step / 1e9, l2 / 1e6)
+                   if bytes_step > 2 * l2 else
+                   "working set %.0f MB is within 2x the %.0f MB L2: L2-resident, not an HBM figure"
+                   % (bytes_step / 1e6, l2 / 1e6)),
             "storage": "bf16 gradients/params, fp32 master/m/v",
         },
         "params_per_s": round(info["elems_per_step"] * nproc / (ms_per_step * 1e-3), 1),
@@ -727,10 +729,64 @@ def cpu_baseline(units, info, bufs, rank, torch, seconds=10.0, n_s=1 << 22):
         if time.perf_counter() - t0 >= seconds:
             break
     dt = time.perf_counter() - t0
-    return {"value": round(per * reps / dt / 1e9, 4), "unit": UNIT, "cores": 1, "kind": "oracle",
-            "sample": "unit 0 (one Llama block) of the workload, first %d elements of rank %d's "
-                      "shard (W=%d), %d repetitions in %.1f s; same algorithmic bytes per element"
-                      % (n_s, rank, W, reps, dt)}
+    out = {"value": round(per * reps / dt / 1e9, 4), "unit": UNIT, "cores": 1, "kind": "oracle",
+           "sample": "unit 0 (one Llama block) of the workload, first %d elements of rank %d's "
+                     "shard (W=%d), %d repetitions in %.1f s; same algorithmic bytes per element"
+                     % (n_s, rank, W, reps, dt),
+           "cpu": cpu_model()}
+    out["all_cores"] = cpu_baseline_all_cores(ora, grads, master, m, v, others, rank, n_s, per, seconds)
+    return out
+
+
+def host_cores():
+    return len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else (os.cpu_count() or 1)
+
+
+def cpu_model():
+    """The host CPU as /proc/cpuinfo names it (Arm cores by their part number)."""
+    arm_parts = {"0xd4f": "Arm Neoverse-V2", "0xd40": "Arm Neoverse-V1", "0xd0c": "Arm Neoverse-N1",
+                 "0xd49": "Arm Neoverse-N2", "0xd8e": "Arm Neoverse-N3", "0xd84": "Arm Neoverse-V3"}
+    try:
+        text = open("/proc/cpuinfo").read()
+    except OSError:
+        return "unknown"
+    for line in text.splitlines():
+        if line.startswith("model name"):
+            return line.split(":", 1)[1].strip()
+    for line in text.splitlines():
+        if line.startswith("CPU part"):
+            part = line.split(":", 1)[1].strip()
+            return arm_parts.get(part, "Arm CPU part " + part)
+    return "unknown"
+
+
+def cpu_baseline_all_cores(ora, grads, master, m, v, others, rank, n_s, per, seconds):
+    """The same oracle step run by one thread per host core, each on its own copy of the
+    sample's state (the C oracle runs without the interpreter lock, so the threads run in
+    parallel); the gradient rows and other ranks' shards are shared read-only."""
+    import threading
+    cores = host_cores()
+    counts = [0] * cores
+
+    def work(i):
+        mp, mm, mv = master.copy(), m.copy(), v.copy()
+        t_end = time.perf_counter() + seconds
+        while True:
+            run_oracle_step(ora, grads, mp, mm, mv, others, rank, n_s, counts[i] + 1)
+            counts[i] += 1
+            if time.perf_counter() >= t_end:
+                break
+
+    threads = [threading.Thread(target=work, args=(i,)) for i in range(cores)]
+    t0 = time.perf_counter()
+    for t in threads:
+        t.start()
+    for t in threads:
+        t.join()
+    dt = time.perf_counter() - t0
+    return {"value": round(per * sum(counts) / dt / 1e9, 4), "unit": UNIT, "cores": cores,
+            "sample": "the same sample, one thread per core on its own copy of the state, %d steps "
+                      "in %.1f s" % (sum(counts), dt)}
 
 
 # ----------------------------------------------------------- reference arm
