@@ -242,10 +242,14 @@ def build_all_ranks(wl, F, torch, fs, synth):
     return units, info, keep
 
 
-def build_sweep(n, W, torch, fs, synth):
+def sweep_workload(n, W):
+    """One FlatParameter of n elements at W ranks (the size sweep of the 7B configuration)."""
     from synth.workloads import Workload
-    wl = Workload("sweep", 6, [[(n,)]], W, sigma_state=1e-4)
-    return build_all_ranks(wl, W, torch, fs, synth)
+    return Workload("sweep", 6, [[(n,)]], W, sigma_state=1e-4)
+
+
+def build_sweep(n, W, torch, fs, synth):
+    return build_all_ranks(sweep_workload(n, W), W, torch, fs, synth)
 
 
 # ------------------------------------------------------------ the GPU arm

@@ -56,13 +56,14 @@ def oracle_at(ora, grad_rows, master, m, v, step):
     return p, mm, vv, bf
 
 
-def check_all_ranks_unit(ora, wl, u, unit, F, before, step, seed):
-    """Sampled parity for one all-ranks unit; `before` holds host draws of the inputs."""
+def check_all_ranks_unit(ora, wl, u, unit, F, before, step, seed, extra_global=()):
+    """Sampled parity for one all-ranks unit; `before` holds host draws of the inputs.
+    `extra_global` adds positions (indices into the flat buffer) to every shard holding them."""
     lay = unit["layout"]
     W, S, P = lay.world_size, lay.shard_numel, lay.numel
     R = W // F
     for p in range(F):
-        j = sample_positions(S, seed=seed + p)
+        j = sample_positions(S, [x - p * S for x in extra_global if 0 <= x - p * S < S], seed=seed + p)
         i = p * S + j
         rows = [synth.normal_bf16_at(wls.key_grad(wl, u, k, 0), i, wl.sigma_grad, n_valid=P) for k in range(W)]
         master = synth.normal_f32_at(wls.key_master(wl, u), i, wl.sigma_master, n_valid=P)
@@ -124,6 +125,32 @@ def test_hybrid_full_size_identical_across_F(ora):
             check_all_ranks_unit(ora, wl, 0, units[0], F, None, 1, seed=21)
         del units, keep, grads, st, full
         torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("W,F,S", [(2, 1, (1 << 31) + 4112), (8, 8, (1 << 28) + 520)])
+def test_flat_parameter_beyond_2_to_the_31_elements(ora, W, F, S):
+    """One FlatParameter of more than 2^31 elements, every rank stepped in one launch.
+    W = 2, F = 1 (the LDG form, two replicas): each shard is the whole padded buffer, so
+    the kernel's element index itself passes 2^31. W = 8, F = 8 (the TMA form): the
+    shards start beyond 2^31 elements of the gradient rows and the full buffer. Both
+    have a ragged last chunk (S mod 2048 != 0) and padding at the end; samples around
+    2^31, 2^30 and both ends of every shard are checked against the oracle."""
+    torch = gu.torch()
+    padded = F * S
+    n = padded - (1 if W == 2 else 5)
+    assert padded > (1 << 31) and S % 8 == 0 and S % 2048 != 0 and padded % W == 0
+    wl = bench.sweep_workload(n, W)
+    units, info, keep = bench.build_all_ranks(wl, F, torch, fs, synth)
+    lay = units[0]["layout"]
+    assert (lay.numel, lay.padded_numel, lay.shard_numel) == (n, padded, S)
+    launches, tma = fs.fsdp_shard_step_grouped_plan(units, 0, W)
+    assert (launches, tma) == (1, 1 if W == 8 else 0)
+    fs.fsdp_shard_step_grouped(units, 0, W, gu.adam_hyper(1))
+    torch.cuda.synchronize()
+    edges = [(1 << 31) + d for d in (-2, -1, 0, 1, 2)] + [n - 1, n, padded - 1, (1 << 30) - 1, 1 << 30]
+    check_all_ranks_unit(ora, wl, 0, units[0], F, None, 1, seed=40 + W, extra_global=edges)
+    del units, keep
+    torch.cuda.empty_cache()
 
 
 def test_llama7b_local_rank(ora):
