@@ -312,6 +312,7 @@ def run_ours(args):
     if dist:
         dist.barrier()
     torch.cuda.synchronize()
+    fs.fsdp_device_status(clear=True)
     clocks.start()
     time.sleep(0.3)
     # one event pair around the whole timed region: events between launches would
@@ -323,6 +324,9 @@ def run_ours(args):
     stream.record_event(stop)
     torch.cuda.synchronize()
     clk = clocks.stop()
+    if fs.fsdp_device_status() != 0:
+        raise RuntimeError("a bounded device wait ran out during the timed steps: blocks stopped early, "
+                           "so the timing is not of the whole step")
     if dist:
         dist.barrier()
     local_ms = start.elapsed_time(stop)

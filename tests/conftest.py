@@ -16,3 +16,24 @@ def pytest_configure(config):
 def ora():
     import oracle
     return oracle.load()
+
+
+@pytest.fixture(autouse=True)
+def _device_status_stays_clear(request):
+    """Every GPU test ends with the device status word clear: no bounded wait of
+    the TMA form ran out (a block that gives up leaves its chunks unprocessed)."""
+    if request.node.get_closest_marker("gpu") is None:
+        yield
+        return
+    try:
+        import torch
+        if not torch.cuda.is_available():
+            yield
+            return
+        import fully_sharded_gb300 as fs
+    except ImportError:
+        yield
+        return
+    fs.fsdp_device_status(clear=True)
+    yield
+    assert fs.fsdp_device_status() == 0, "a bounded device wait ran out during this test"
