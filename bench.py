@@ -390,7 +390,8 @@ def run_ours(args):
     if not args.no_e2e and name == "llama7b" and not args.units:
         line["e2e"] = e2e_local_rank(args, torch, fs, synth, wls.LLAMA7B, units, info, bufs, rb, stream,
                                      nproc, dist)
-    if rank == 0 and not args.no_cpu_baseline and name == "llama7b":
+    # the oracle baseline: rank 0 of a one-GPU run only
+    if world == 1 and rank == 0 and not args.no_cpu_baseline and name == "llama7b":
         line["cpu_baseline"] = cpu_baseline(units, info, bufs, rb, torch, seconds=args.cpu_seconds)
     if dist:
         dist.destroy_process_group()
