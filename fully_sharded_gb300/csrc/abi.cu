@@ -389,6 +389,9 @@ extern "C" int fsdp_shard_step_grouped_plan(const fsdp_unit_args_t* units, int32
 
 extern "C" int fsdp_device_status(int32_t clear, uint32_t* status_out) {
   if (!status_out) return FSDP_EINVAL;
+  // the symbol copy runs on the legacy default stream, which does not wait for
+  // non-blocking streams: finish all work of the device first
+  if (cudaDeviceSynchronize() != cudaSuccess) return FSDP_ECUDA;
   unsigned int v = 0;
   if (cudaMemcpyFromSymbol(&v, g_fsdp_status, sizeof(v)) != cudaSuccess) return FSDP_ECUDA;
   if (clear) {

@@ -217,7 +217,8 @@ int fsdp_shard_step_grouped_plan(const fsdp_unit_args_t *units, int32_t n_units,
                                  int32_t rank_begin, int32_t rank_end, int32_t *launches_out,
                                  int32_t *tma_launches_out);
 
-/* The current device's sticky status word (synchronizes the device). Bit 0 is
+/* The current device's sticky status word, read after all work of the
+ * device, on every stream, has finished (the call synchronizes the device). Bit 0 is
  * set when a bounded wait of the TMA form ran out (2 s on one mbarrier): the
  * block that saw it stopped early, so the outputs of that launch are not
  * valid. This does not happen in a correct run. clear != 0 resets the word
