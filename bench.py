@@ -288,10 +288,12 @@ def run_ours(args):
         rb, re = 0, wl.world_size
         workload_name = "hybrid_W16_F%d" % F
     elif name.startswith("sweep"):
-        # sweep_<n>_W<w>
-        _, n, w = name.split("_")
-        units, info, bufs = build_sweep(int(float(n)), int(w[1:]), torch, fs, synth)
-        rb, re = 0, int(w[1:])
+        # sweep_<n>_W<w>, or sweep_<n>_W<w>_F<f> for a hybrid step (F | W, R = W / F replicas)
+        parts = name.split("_")
+        n, W = int(float(parts[1])), int(parts[2][1:])
+        F = int(parts[3][1:]) if len(parts) > 3 else W
+        units, info, bufs = build_all_ranks(sweep_workload(n, W), F, torch, fs, synth)
+        rb, re = 0, W
         workload_name = name
     else:
         raise SystemExit("unknown workload %s" % name)
