@@ -26,6 +26,7 @@ __all__ = [
     "fsdp_shard_step_grouped_launches", "fsdp_pipeline_step", "PipelineUnit", "PipelineBatch",
     "fsdp_pipeline_step_noalloc", "fsdp_all_gather_state", "fsdp_zero1_step", "fsdp_account_zero",
     "fsdp_shard_step_grouped_plan", "fsdp_device_status", "fsdp_selftest_wait_timeout",
+    "fsdp_offload_step", "OffloadUnit", "OffloadBatch",
 ]
 
 FSDP_OK = 0
@@ -69,6 +70,11 @@ class PipelineUnit(ctypes.Structure):
     _fields_ = [("layout", ctypes.POINTER(Layout)), ("grad_slices", _c_p), ("master", _c_p),
                 ("exp_avg", _c_p), ("exp_avg_sq", _c_p), ("other_shards", _c_p), ("full_out", _c_p),
                 ("shard_out", _c_p)]
+
+
+class OffloadUnit(ctypes.Structure):
+    _fields_ = [("layout", ctypes.POINTER(Layout)), ("grads", _c_p), ("master", _c_p), ("exp_avg", _c_p),
+                ("exp_avg_sq", _c_p), ("other_shards", _c_p), ("full_out", _c_p)]
 
 
 class ZeroAccount(ctypes.Structure):
@@ -131,6 +137,8 @@ def _load():
                                          ctypes.POINTER(_c_i32), ctypes.POINTER(_c_i32)],
         "fsdp_device_status": [_c_i32, ctypes.POINTER(ctypes.c_uint32)],
         "fsdp_selftest_wait_timeout": [P, P, _c_i64, _c_i64, P, ctypes.POINTER(ctypes.c_uint32)],
+        "fsdp_offload_step": [ctypes.POINTER(OffloadUnit), _c_i32, _c_i32, P, _c_i64, _c_i32,
+                              ctypes.POINTER(AdamHyper), P, P, P],
     }
     for name, args in sigs.items():
         fn = getattr(lib, name)
@@ -334,6 +342,42 @@ def fsdp_pipeline_step(units, rank: int, staging, slot_numel: int, n_slots: int,
     _check("fsdp_pipeline_step", _lib.fsdp_pipeline_step(
         batch.array, batch.n, rank, _dptr(staging, 2), slot_numel, n_slots, ctypes.byref(adam),
         _stream(compute), _stream(copy)))
+
+
+class OffloadBatch:
+    """Marshalled units for fsdp_offload_step (kept alive together)."""
+
+    def __init__(self, units):
+        self._keep = []
+        self.array = (OffloadUnit * max(1, len(units)))()
+        self.n = len(units)
+        for i, u in enumerate(units):
+            lay = u["layout"]
+            g = _parray(u["grads"], 2)
+            oth = _parray(u["other_shards"], 2)
+            self._keep.append((lay, g, oth))
+            a = self.array[i]
+            a.layout = ctypes.pointer(lay)
+            a.grads = ctypes.cast(g, _c_p)
+            for name in ("master", "exp_avg", "exp_avg_sq"):
+                x = u[name]
+                if x is not None and not isinstance(x, int) and x.element_size() != 4:
+                    raise ValueError("%s: expected fp32, got %s" % (name, x.dtype))
+                setattr(a, name, _addr(x))
+            a.other_shards = ctypes.cast(oth, _c_p)
+            a.full_out = _dptr(u["full_out"], 2)
+
+
+def fsdp_offload_step(units, rank: int, staging, slot_numel: int, n_slots: int, adam: AdamHyper,
+                      compute=None, h2d=None, d2h=None):
+    """Staged optimizer-state offload over many units: `units` are dicts (layout, grads,
+    master, exp_avg, exp_avg_sq, other_shards, full_out) with master/exp_avg/exp_avg_sq in
+    (pinned) host memory, or an OffloadBatch; `staging`: device fp32 buffer of
+    n_slots * 3 * slot_numel."""
+    batch = units if isinstance(units, OffloadBatch) else OffloadBatch(units)
+    _check("fsdp_offload_step", _lib.fsdp_offload_step(
+        batch.array, batch.n, rank, _dptr(staging, 4), slot_numel, n_slots, ctypes.byref(adam),
+        _stream(compute), _stream(h2d), _stream(d2h)))
 
 
 def fsdp_pipeline_step_noalloc(units, rank: int, n_slots: int, adam: AdamHyper, compute=None,

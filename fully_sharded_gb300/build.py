@@ -13,7 +13,7 @@ INCLUDE = os.path.join(ROOT, "include")
 OUT_DIR = os.path.join(PKG, "_build")
 SO = os.path.join(OUT_DIR, "libfsdp_gb300.so")
 
-SOURCES = ["abi.cu", "pipeline.cu", "noalloc.cu", "state.cu", "host_layout.cpp"]
+SOURCES = ["abi.cu", "pipeline.cu", "noalloc.cu", "state.cu", "offload.cu", "host_layout.cpp"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-I", INCLUDE, "-I", CSRC]
 

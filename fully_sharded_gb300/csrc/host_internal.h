@@ -101,6 +101,22 @@ class AliasCheck {
 };
 
 
+// Events of one scheduler call: created on construction, released on
+// destruction (the runtime releases a pending event once it completes).
+struct EventSet {
+  std::vector<cudaEvent_t> ev;
+  bool ok = true;
+  explicit EventSet(int n) : ev(n, nullptr) {
+    for (auto& e : ev) ok = ok && cudaEventCreateWithFlags(&e, cudaEventDisableTiming) == cudaSuccess;
+  }
+  ~EventSet() {
+    for (auto e : ev)
+      if (e) cudaEventDestroy(e);
+  }
+  EventSet(const EventSet&) = delete;
+  EventSet& operator=(const EventSet&) = delete;
+};
+
 // Launch the list, splitting it where a descriptor table would overflow. With
 // `count` set, nothing is launched and the number of launches is returned there.
 // `tma_count`, if set, receives how many of those launches use the TMA form.

@@ -20,20 +20,6 @@ namespace {
 
 constexpr int kMaxSlots = 8;
 
-// Creates events on construction and releases them on destruction (a pending
-// event is released by the runtime once it completes).
-struct EventSet {
-  std::vector<cudaEvent_t> ev;
-  bool ok = true;
-  explicit EventSet(int n) : ev(n, nullptr) {
-    for (auto& e : ev) ok = ok && cudaEventCreateWithFlags(&e, cudaEventDisableTiming) == cudaSuccess;
-  }
-  ~EventSet() {
-    for (auto e : ev)
-      if (e) cudaEventDestroy(e);
-  }
-};
-
 // Segments of one unit's local-rank step with the gradients in a staging slot.
 void unit_segments(const fsdp_pipeline_unit_t& u, int rank, const uint16_t* slot, SegmentList& list) {
   const fsdp_layout_t* L = u.layout;

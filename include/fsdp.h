@@ -277,6 +277,54 @@ int fsdp_pipeline_step(const fsdp_pipeline_unit_t *units, int32_t n_units, int32
                        uint16_t *staging, int64_t slot_numel, int32_t n_slots,
                        const fsdp_adam_t *adam, fsdp_stream_t compute, fsdp_stream_t copy);
 
+/* Staged optimizer-state offload: one rank's step over many units (full
+ * sharding, F = W) with that rank's fp32 master, exp_avg and exp_avg_sq
+ * shards in host memory.
+ * [gloss] "CPU Offload" (optimizer state held in CPU memory and brought to the
+ * GPU for the update); [math] "The backward cycle: all-gather, grads,
+ * reduce-scatter" (the per-unit step it wraps).
+ * For unit u in order, slot s = u mod n_slots of `staging`:
+ *   on `h2d`:     wait until the unit that last used slot s is back in host
+ *                 memory, then copy the unit's master, exp_avg, exp_avg_sq
+ *                 (S fp32 each) into slot s;
+ *   on `compute`: wait for those copies, run the fused local-rank step of
+ *                 `rank` on the state in slot s (reduce-scatter of the rank's
+ *                 slice of the W gradient rows, Adam, bf16 cast into full_out,
+ *                 all-gather of the other ranks' shards into full_out);
+ *   on `d2h`:     wait for the step, copy the three updated shards back to
+ *                 host memory.
+ * With n_slots >= 2 the copy in of unit u+1, the step of unit u and the copy
+ * back of unit u-1 overlap, so both directions of the host link are busy at
+ * once (the zero-copy form of the conventions above moves the same state by
+ * kernel loads and stores instead).
+ * staging: device fp32 buffer of n_slots x 3 x slot_numel, caller-owned,
+ * contents overwritten; slot_numel >= shard_numel of every unit (a multiple
+ * of 4 keeps every slot array 16-byte aligned, the vector path). n_slots in
+ * [1, 8]. master/exp_avg/exp_avg_sq: host memory, page-locked for the copies
+ * to overlap (pageable memory works but each copy then waits for the host);
+ * device memory also works. When the call returns, `compute` and `h2d` are
+ * ordered after the last copy back, so later work on any of the three streams
+ * sees the updated state. The streams may coincide (no overlap). Results are
+ * bit-identical to fsdp_shard_step_grouped with the same state in HBM.
+ * EINVAL: F != W, a unit with another W, bad rank, n_slots outside [1,8], a
+ * slot too small, null pointers; EALIAS: outputs (state, full_out, staging)
+ * overlapping inputs or each other. */
+typedef struct {
+  const fsdp_layout_t *layout;
+  const uint16_t *const *grads;        /* W device bf16 rows of padded_numel (rank k's
+                                          gradient); the step reads the owned slice */
+  float *master;                       /* fp32 [S] of the owned rank, host memory, in place */
+  float *exp_avg;                      /* fp32 [S], host memory, in place */
+  float *exp_avg_sq;                   /* fp32 [S], host memory, in place */
+  const uint16_t *const *other_shards; /* W device pointers by rank; the owned rank's entry
+                                          is ignored */
+  uint16_t *full_out;                  /* device bf16 [padded_numel] */
+} fsdp_offload_unit_t;
+
+int fsdp_offload_step(const fsdp_offload_unit_t *units, int32_t n_units, int32_t rank, float *staging,
+                      int64_t slot_numel, int32_t n_slots, const fsdp_adam_t *adam,
+                      fsdp_stream_t compute, fsdp_stream_t h2d, fsdp_stream_t d2h);
+
 /* Allocation-free form of fsdp_pipeline_step. (The FSDP pages have no
  * counterpart: this exists for callers, not for the method.)
  * For callers that cannot allocate device memory where they step the

@@ -252,6 +252,34 @@ def test_pipeline_rejects_bad_arguments():
     call(fs.FSDP_EALIAS, units=[unit, dict(unit, grad_slices=_addr(30))])  # two units, same outputs
 
 
+def test_offload_rejects_bad_arguments():
+    W, S = 4, 256
+    lay = _lay(W * S, W)
+    unit = dict(layout=lay, grads=[_addr(1 + k) for k in range(W)], master=_addr(10), exp_avg=_addr(11),
+                exp_avg_sq=_addr(12), other_shards=[_addr(20 + k) for k in range(W)], full_out=_addr(30))
+
+    def call(status, units=None, rank=0, staging=_addr(40), slot=S, n_slots=2, adam=HP):
+        with pytest.raises(FsdpError) as e:
+            fs.fsdp_offload_step([unit] if units is None else units, rank, staging, slot, n_slots, adam,
+                                 compute=0, h2d=0, d2h=0)
+        assert e.value.status == status
+
+    call(fs.FSDP_EINVAL, n_slots=0)
+    call(fs.FSDP_EINVAL, n_slots=9)
+    call(fs.FSDP_EINVAL, slot=S - 1)
+    call(fs.FSDP_EINVAL, rank=W)
+    call(fs.FSDP_EINVAL, rank=-1)
+    call(fs.FSDP_EINVAL, units=[dict(unit, layout=_lay(W * S, W, 2))])     # hybrid layout
+    call(fs.FSDP_EINVAL, units=[dict(unit, master=None)])
+    call(fs.FSDP_EINVAL, units=[dict(unit, grads=unit["grads"][:3] + [None])])
+    call(fs.FSDP_EINVAL, units=[dict(unit, other_shards=[_addr(20), None, _addr(22), _addr(23)])])
+    call(fs.FSDP_EINVAL, units=[unit, dict(unit, layout=_lay(8 * S, 8))])  # another W
+    call(fs.FSDP_EALIAS, staging=_addr(10))                                # staging over the master shard
+    call(fs.FSDP_EALIAS, units=[dict(unit, exp_avg=_addr(10) + 512)])      # m overlapping master
+    call(fs.FSDP_EALIAS, units=[dict(unit, full_out=_addr(2) + 16)])       # full_out over a gradient row
+    call(fs.FSDP_EALIAS, units=[unit, dict(unit, grads=[_addr(50 + k) for k in range(W)])])  # same outputs
+
+
 def test_account_zero_matches_oracle_and_golden(ora):
     for P in (0.0, 1.0, 7e9, 124439808.0):
         for N in (1, 2, 8, 64):

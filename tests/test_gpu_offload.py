@@ -51,3 +51,53 @@ def test_state_in_host_memory_matches_oracle(ora, W, P, rank):
         gu.assert_same_bits(he[i].numpy(), oe[i], "exp_avg")
         gu.assert_same_bits(hv[i].numpy(), ov[i], "exp_avg_sq")
     gu.assert_same_bits(gu.to_host(full), ofull[0], "full")
+
+
+@pytest.mark.parametrize("n_slots,same_stream,odd_slot", [(1, False, False), (2, False, False),
+                                                          (3, False, False), (2, True, False),
+                                                          (2, False, True)])
+def test_staged_offload_matches_oracle(ora, n_slots, same_stream, odd_slot):
+    """fsdp_offload_step over four units (a ragged one, whole chunks, a larger one, a tiny
+    one), W = 8, rank 5, two steps in a row with fresh gradients: the host state and every
+    full buffer equal the oracle's bit for bit. odd_slot: slot arrays not 16-byte aligned
+    (the scalar path)."""
+    torch = gu.torch()
+    W, rank = 8, 5
+    sizes = [8 * 40000 + 5, 8 * 2048 * 3, 8 * 100000, 17]
+    lays = [fs.fsdp_flatten_layout([P], W)[0] for P in sizes]
+    pin = lambda a: torch.from_numpy(a.copy()).pin_memory()  # noqa: E731
+    units, oracle_units = [], []
+    for u, (P, lay) in enumerate(zip(sizes, lays)):
+        S, padded = lay.shard_numel, lay.padded_numel
+        base = 4500 + u
+        sl = lambda a: np.ascontiguousarray(a[rank * S:(rank + 1) * S])  # noqa: E731
+        master = synth.normal_f32(synth.stream_key(base, 1), padded, 0.02, n_valid=P)
+        m = synth.normal_f32(synth.stream_key(base, 2), padded, 1e-4, absval=True, n_valid=P)
+        v = synth.normal_f32(synth.stream_key(base, 3), padded, 1e-4, absval=True, n_valid=P)
+        others = [synth.normal_bf16(synth.stream_key(base, 5), S, 0.02, idx0=k * S) for k in range(W)]
+        units.append(dict(layout=lay, master=pin(sl(master)), exp_avg=pin(sl(m)), exp_avg_sq=pin(sl(v)),
+                          other_shards=[gu.to_dev(o) for o in others],
+                          full_out=torch.zeros(padded, dtype=torch.int16, device="cuda")))
+        oracle_units.append(dict(master=sl(master).copy(), m=sl(m).copy(), v=sl(v).copy(), others=others,
+                                 full=np.zeros(padded, np.uint16), base=base, P=P, padded=padded))
+    slot = max(l.shard_numel for l in lays)
+    slot = slot + (1 if slot % 4 == 0 else 0) if odd_slot else (slot + 3) // 4 * 4
+    staging = torch.empty(n_slots * 3 * slot, device="cuda")
+    streams = [torch.cuda.Stream()] * 3 if same_stream else [torch.cuda.Stream() for _ in range(3)]
+    for step in (1, 2):
+        for u, o in zip(units, oracle_units):
+            g = [synth.normal_bf16(synth.stream_key(o["base"], 4, k, step), o["padded"], 1e-2, n_valid=o["P"])
+                 for k in range(W)]
+            u["grads"] = [gu.to_dev(x) for x in g]
+            o["grads"] = g
+        fs.fsdp_offload_step(units, rank, staging, slot, n_slots, gu.adam_hyper(step),
+                             compute=streams[0], h2d=streams[1], d2h=streams[2])
+        streams[0].synchronize()  # ordered after every copy back
+        for o in oracle_units:
+            ora.shard_step(o["grads"], W, rank, rank + 1, [o["master"]], [o["m"]], [o["v"]], o["others"],
+                           [o["full"]], step=step, **gu.HP)
+        for i, (u, o) in enumerate(zip(units, oracle_units)):
+            gu.assert_same_bits(u["master"].numpy(), o["master"], "master u%d step %d" % (i, step))
+            gu.assert_same_bits(u["exp_avg"].numpy(), o["m"], "exp_avg u%d step %d" % (i, step))
+            gu.assert_same_bits(u["exp_avg_sq"].numpy(), o["v"], "exp_avg_sq u%d step %d" % (i, step))
+            gu.assert_same_bits(gu.to_host(u["full_out"]), o["full"], "full u%d step %d" % (i, step))
