@@ -10,10 +10,11 @@
 // consumers from global memory as in segment_kernel.
 //
 // Measured on GB300 against segment_kernel (same chunks, same arithmetic,
-// bit-identical results): W = 8 single-replica launches gain 1-4 % (Llama
-// block 1.246 -> 1.206 ms); W <= 4, replica-heavy hybrid steps and short
-// launches lose, so the host uses this form only for W = 8 launches with one
-// replica per position and at least kTmaMinChunksPerBlock chunks per block.
+// bit-identical results): W = 8 single-replica step launches gain 1-4 %
+// (Llama block 1.246 -> 1.206 ms); W <= 4, replica-heavy hybrid steps, short
+// launches and launches of reduce chunks lose, so the host uses this form only
+// for W = 8 launches made of one-replica step segments (and copies) with at
+// least kTmaMinChunksPerBlock chunks per block.
 //
 // Every mbarrier wait is bounded in time (Params::wait_limit_ns, read from
 // %globaltimer): when a wait runs out the block sets bit 0 of g_fsdp_status,
