@@ -4,8 +4,9 @@
 // The producer (lane 0 of warp 8) stages each eligible chunk with
 // cp.async.bulk (global -> shared; completion counted in bytes on the stage's
 // "full" mbarrier) up to kStages chunks ahead; the consumer warps wait on
-// that barrier, run the fused step (or the copy) from shared memory, store to
-// global memory and release the stage on its "empty" mbarrier. Chunks that
+// that barrier, run the fused step from shared memory and store its results
+// to global memory (a staged copy chunk goes back out as one bulk store,
+// shared -> global), then release the stage on its "empty" mbarrier. Chunks that
 // cannot be staged (misaligned segments, other kinds) are run by the
 // consumers from global memory as in segment_kernel.
 //
@@ -91,6 +92,18 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
                "l"(src), "r"(bytes), "r"(bar)
                : "memory");
 }
+
+// Bulk store of `bytes` from shared memory (16-byte aligned) to global memory
+// (16-byte aligned, bytes a multiple of 16), as its own bulk async-group.
+__device__ __forceinline__ void bulk_store(void* dst, uint32_t src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst), "r"(src), "r"(bytes)
+               : "memory");
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+// The issuing thread's bulk stores have finished reading shared memory.
+__device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+// The issuing thread's bulk stores have completed their writes.
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
 // Waits for the phase of `parity` to complete. False when the block aborted
 // or the time limit ran out (then the abort flag and the status word are set).
@@ -197,20 +210,21 @@ __device__ __forceinline__ void tma_consume_step(const Params& p, const Seg& d, 
   }
 }
 
-__device__ __forceinline__ void tma_consume_copy(const Params& p, const Seg& d, int64_t local,
-                                                 const unsigned char* stage, int64_t nb) {
+// A staged copy chunk goes back out as one bulk store issued by thread 0, so
+// the consumer warps never handle copy data; the thread copies the chunk's
+// last < 16 bytes itself and waits until the store has read the stage before
+// its warp releases it.
+__device__ __forceinline__ void tma_store_copy(const Params& p, const Seg& d, int64_t local,
+                                               const unsigned char* stage, int64_t nb) {
+  if (threadIdx.x != 0) return;
   const int64_t b0 = local * kChunkBytes;
   unsigned char* dst = static_cast<unsigned char*>(const_cast<void*>(p.ptr[d.ptr + 1]));
-#pragma unroll
-  for (int k = 0; k < kCopyVecs; ++k) {
-    const int64_t b = (int64_t(k) * kThreads + threadIdx.x) * 16;
-    if (b + 16 <= nb) st_stream_u4(dst + b0 + b, *reinterpret_cast<const uint4*>(stage + b));
-  }
-  if (threadIdx.x == 0) {  // the last < 16 bytes of the chunk
-    const unsigned char* src = static_cast<const unsigned char*>(p.ptr[d.ptr]);
-    const int64_t end = (b0 + kChunkBytes < d.n) ? b0 + kChunkBytes : d.n;
-    for (int64_t q = b0 + nb; q < end; ++q) dst[q] = src[q];
-  }
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+  bulk_store(dst + b0, sm_addr(stage), static_cast<uint32_t>(nb));
+  const unsigned char* src = static_cast<const unsigned char*>(p.ptr[d.ptr]);
+  const int64_t end = (b0 + kChunkBytes < d.n) ? b0 + kChunkBytes : d.n;
+  for (int64_t q = b0 + nb; q < end; ++q) dst[q] = src[q];
+  bulk_wait_read_all();
 }
 
 template <int W>
@@ -278,7 +292,7 @@ __global__ void __launch_bounds__(kTmaThreads, 1) tma_kernel(const __grid_consta
     if (bytes != 0 && d.kind == kStep) {
       tma_consume_step<W>(p, d, l, st, staged);
     } else if (bytes != 0) {
-      tma_consume_copy(p, d, l, st, staged);
+      tma_store_copy(p, d, l, st, staged);
     } else {
       switch (d.kind) {
         case kStep: step_chunk<W>(p, d, l * kChunkElems); break;
@@ -291,6 +305,7 @@ __global__ void __launch_bounds__(kTmaThreads, 1) tma_kernel(const __grid_consta
     __syncwarp();
     if (lane == 0) mbar_arrive(sm_addr(&empty_bar[stage]));
   }
+  if (threadIdx.x == 0) bulk_wait_all();  // every bulk store written before the block exits
 }
 
 }  // namespace fsdp
