@@ -492,7 +492,7 @@ def host_link(torch, stream, nbytes=1 << 31, reps=3):
 
 
 def run_unfused(args):
-    """Rows a3, a4, a6 and a2 timed on their own on the Llama block (W = 8, all ranks):
+    """The step's parts as separate calls, timed on the Llama block (W = 8, all ranks):
     per rank fsdp_reduce_scatter (fp32 gradient shard out) and fsdp_adam_shard_step
     (bf16 shard out), then fsdp_all_gather of the 8 shards; against the fused step on
     the same buffers. Also fsdp_pack_flat of the block's nine fp32 tensors."""
@@ -645,7 +645,7 @@ def run_offload(args):
 
 
 def run_state(args):
-    """NEXT-2 / NEXT-3 rows timed on the Llama block (W = 8): the ZeRO-1 step of rank 0
+    """The optimizer-state entry points timed on the Llama block (W = 8): the ZeRO-1 step of rank 0
     (full all-reduce average kept, then the rank's Adam and gather) against the fused
     local-rank step on the same buffers, and the full-state gather + unflatten of the
     fp32 master (8 shards -> flat -> 9 tensors)."""

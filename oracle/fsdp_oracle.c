@@ -10,6 +10,18 @@
  * Build: gcc -O2 -std=c11 -ffp-contract=off -fno-fast-math -shared -fPIC
  * (no FMA contraction: every fp32 operation below rounds once, IEEE RNE).
  *
+ * The steps are labelled throughout the sources as follows:
+ *   a1  flatten layout: tensor offsets, padding to a multiple of W, shard length
+ *   a2  pack / unpack: tensors into the flat buffer (pad zeroed) and back
+ *   a3  reduce-scatter: fp32 fold of the W bf16 rows in rank order, divided
+ *       by W, at the rank's shard
+ *   a4  Adam on a shard, in place (fp32 master, exp_avg, exp_avg_sq)
+ *   a5  bf16 cast of the updated master shard
+ *   a6  all-gather: the bf16 shards into the full FlatParameter
+ *   a7  the fused step: a3 -> a4 -> a5 -> a6 in one pass
+ *   a8  hybrid sharding (F | W): shard within groups of F, W / F replicas
+ *   a9  closed-form memory and communication accountant
+ *
  * Sources (web pages on PyTorch FSDP; cited by page and section):
  *   [notes]   "NOTE-003: PyTorch FSDP" (reading notes on the FSDP paper)
  *   [math]    "transformer math: FSDP" (FlatParameter, cycles, budgets, worked example)
