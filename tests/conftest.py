@@ -10,6 +10,10 @@ if ROOT not in sys.path:
 
 def pytest_configure(config):
     config.addinivalue_line("markers", "gpu: needs a CUDA GPU (sm_103a); run with -m gpu")
+    # compile whatever native part is missing or older than its sources (the CUDA
+    # library, the device input generator, the C oracle); nothing when up to date
+    import __graft_entry__
+    __graft_entry__.build()
 
 
 @pytest.fixture(scope="session")
