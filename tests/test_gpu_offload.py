@@ -53,23 +53,22 @@ def test_state_in_host_memory_matches_oracle(ora, W, P, rank):
     gu.assert_same_bits(gu.to_host(full), ofull[0], "full")
 
 
-@pytest.mark.parametrize("n_slots,same_stream,odd_slot", [(1, False, False), (2, False, False),
-                                                          (3, False, False), (2, True, False),
-                                                          (2, False, True)])
-def test_staged_offload_matches_oracle(ora, n_slots, same_stream, odd_slot):
+@pytest.mark.parametrize("W,rank,n_slots,same_stream,odd_slot", [
+    (8, 5, 1, False, False), (8, 5, 2, False, False), (8, 5, 3, False, False), (8, 5, 2, True, False),
+    (8, 5, 2, False, True), (3, 1, 2, False, False)])
+def test_staged_offload_matches_oracle(ora, W, rank, n_slots, same_stream, odd_slot):
     """fsdp_offload_step over four units (a ragged one, whole chunks, a larger one, a tiny
-    one), W = 8, rank 5, two steps in a row with fresh gradients: the host state and every
-    full buffer equal the oracle's bit for bit. odd_slot: slot arrays not 16-byte aligned
-    (the scalar path)."""
+    one), two steps in a row with fresh gradients: the host state and every full buffer
+    equal the oracle's bit for bit. odd_slot: slot arrays not 16-byte aligned (the scalar
+    path); W = 3: shards of odd length, misaligned views (the scalar path as well)."""
     torch = gu.torch()
-    W, rank = 8, 5
     sizes = [8 * 40000 + 5, 8 * 2048 * 3, 8 * 100000, 17]
     lays = [fs.fsdp_flatten_layout([P], W)[0] for P in sizes]
     pin = lambda a: torch.from_numpy(a.copy()).pin_memory()  # noqa: E731
     units, oracle_units = [], []
     for u, (P, lay) in enumerate(zip(sizes, lays)):
         S, padded = lay.shard_numel, lay.padded_numel
-        base = 4500 + u
+        base = 4500 + 10 * W + u
         sl = lambda a: np.ascontiguousarray(a[rank * S:(rank + 1) * S])  # noqa: E731
         master = synth.normal_f32(synth.stream_key(base, 1), padded, 0.02, n_valid=P)
         m = synth.normal_f32(synth.stream_key(base, 2), padded, 1e-4, absval=True, n_valid=P)
