@@ -52,7 +52,7 @@ const void* kernel_of(int variant) {
     case 2: return reinterpret_cast<const void*>(&segment_kernel<4>);
     case 3: return reinterpret_cast<const void*>(&segment_kernel<8>);
     case 4: return reinterpret_cast<const void*>(&segment_kernel<16>);
-    case kTmaVariant: return reinterpret_cast<const void*>(&tma_kernel<8>);
+    case kTmaVariant: return reinterpret_cast<const void*>(&tma_kernel<8, false>);
     default: return reinterpret_cast<const void*>(&segment_kernel<0>);
   }
 }
@@ -76,8 +76,12 @@ int grid_capacity(int variant, int* err) {
   if (per_sm == 0) {
     const bool tma = variant == kTmaVariant;
     const int smem = tma ? TmaCfg<8>::kSmemBytes : 0;
-    if (tma && cudaFuncSetAttribute(kernel_of(variant), cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
-                   cudaSuccess) {
+    // both instantiations of the TMA form (one and four copies per array) get
+    // the shared memory of the pipeline
+    if (tma && (cudaFuncSetAttribute(kernel_of(variant), cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
+                    cudaSuccess ||
+                cudaFuncSetAttribute(reinterpret_cast<const void*>(&tma_kernel<8, true>),
+                                     cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)) {
       *err = FSDP_ECUDA;
       return 0;
     }
@@ -119,7 +123,7 @@ cudaError_t launch_variant(const Params& p, int grid, cudaStream_t stream) {
   return e != cudaSuccess ? e : cudaGetLastError();
 }
 
-cudaError_t launch_tma(const Params& p, int grid, cudaStream_t stream) {
+cudaError_t launch_tma(const Params& p, int grid, cudaStream_t stream, bool interleave = false) {
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(kTmaThreads);
@@ -130,7 +134,8 @@ cudaError_t launch_tma(const Params& p, int grid, cudaStream_t stream) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  const cudaError_t e = cudaLaunchKernelEx(&cfg, tma_kernel<8>, p);
+  const cudaError_t e = interleave ? cudaLaunchKernelEx(&cfg, tma_kernel<8, true>, p)
+                                   : cudaLaunchKernelEx(&cfg, tma_kernel<8, false>, p);
   return e != cudaSuccess ? e : cudaGetLastError();
 }
 
@@ -152,6 +157,31 @@ bool use_tma(const Params& p, int tma_grid) {
     }
   }
   return step && p.total_chunks >= static_cast<int64_t>(kTmaMinChunksPerBlock) * tma_grid;
+}
+
+// A TMA launch whose step segments have gradient rows spanning 4 GiB or more
+// of addresses stages them in interleaved quarter-chunk copies (the second
+// instantiation of the kernel). Measured on GB300 (interleaved A/B): with 8
+// rows 1 GB apart (a 5e8-element FlatParameter, 7 GB span) and 2 GB apart (1e9
+// elements, 14 GB span), one 4 KB copy per row ran 2.1-3.1 % slower than
+// interleaved 1 KB pieces, likely DRAM bank mapping; with spans up to 3.7 GB
+// (GPT-2, the Llama block, the 7B units) interleaving gained nothing, and on
+// GPT-2 its four times as many copies cost 2 %.
+constexpr uintptr_t kInterleaveSpread = uintptr_t(4) << 30;
+
+bool wants_interleave(const Params& p) {
+  for (int k = 0; k < p.nseg; ++k) {
+    const Seg& d = p.seg[k];
+    if (d.kind != kStep) continue;
+    uintptr_t lo = UINTPTR_MAX, hi = 0;
+    for (int r = 0; r < p.s.w; ++r) {
+      const uintptr_t a = reinterpret_cast<uintptr_t>(p.ptr[d.ptr + r]);
+      lo = std::min(lo, a);
+      hi = std::max(hi, a);
+    }
+    if (hi - lo >= kInterleaveSpread) return true;
+  }
+  return false;
 }
 
 }  // namespace
@@ -208,7 +238,8 @@ int launch(const SegmentList& list, const Scalars& s, cudaStream_t stream, int* 
       continue;
     }
     if (tma) {
-      if (launch_tma(p, static_cast<int>(std::min<int64_t>(chunks, tma_cap)), stream) != cudaSuccess)
+      if (launch_tma(p, static_cast<int>(std::min<int64_t>(chunks, tma_cap)), stream, wants_interleave(p)) !=
+          cudaSuccess)
         return FSDP_ECUDA;
       continue;
     }

@@ -10,6 +10,11 @@
 // cannot be staged (misaligned segments, other kinds) are run by the
 // consumers from global memory as in segment_kernel.
 //
+// Two instantiations: kInterleave = false stages a step chunk with one bulk
+// copy per array; kInterleave = true (the host picks it when a launch's
+// gradient rows span 4 GiB or more of addresses) in four rounds of quarter
+// chunks over the arrays.
+//
 // Measured on GB300 against segment_kernel (same chunks, same arithmetic,
 // bit-identical results): W = 8 single-replica step launches gain 1-4 %
 // (Llama block 1.246 -> 1.206 ms); W <= 4, replica-heavy hybrid steps, short
@@ -125,8 +130,10 @@ __device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, volati
 // Bytes staged for a chunk (0: the consumers read it from global memory);
 // issues the bulk copies when `issue` is set. Rows at k * kRowBytes, state
 // array a at W * kRowBytes + a * kStateBytes, copy data at 0. *staged_n is
-// the number of staged elements (step) or bytes (copy).
-template <int W>
+// the number of staged elements (step) or bytes (copy). kInterleave: a step
+// chunk is copied in four rounds over its arrays (a quarter chunk of every row,
+// then of every state array) instead of one copy per array.
+template <int W, bool kInterleave>
 __device__ __forceinline__ uint32_t tma_chunk(const Params& p, const Seg& d, int64_t local, unsigned char* stage,
                                               uint32_t bar, bool issue, uint32_t extra_tx, int64_t* staged_n) {
   *staged_n = 0;
@@ -141,14 +148,29 @@ __device__ __forceinline__ uint32_t tma_chunk(const Params& p, const Seg& d, int
     const uint32_t total = static_cast<uint32_t>(nc * (2 * W + 12));
     if (!issue) return total;
     mbar_expect_tx_arrive(bar, total + extra_tx);
+    if constexpr (kInterleave) {
+      constexpr int64_t kPiece = kChunkElems / 4;
+      for (int64_t q0 = 0; q0 < nc; q0 += kPiece) {
+        const int64_t pe = (nc - q0 < kPiece) ? nc - q0 : kPiece;  // a multiple of 8
 #pragma unroll
-    for (int k = 0; k < W; ++k)
-      bulk_load(sm_addr(stage + k * TmaCfg<W>::kRowBytes), static_cast<const uint16_t*>(p.ptr[d.ptr + k]) + e0,
-                static_cast<uint32_t>(nc * 2), bar);
+        for (int k = 0; k < W; ++k)
+          bulk_load(sm_addr(stage + k * TmaCfg<W>::kRowBytes + q0 * 2),
+                    static_cast<const uint16_t*>(p.ptr[d.ptr + k]) + e0 + q0, static_cast<uint32_t>(pe * 2), bar);
 #pragma unroll
-    for (int a = 0; a < 3; ++a)
-      bulk_load(sm_addr(stage + W * TmaCfg<W>::kRowBytes + a * TmaCfg<W>::kStateBytes),
-                static_cast<const float*>(p.ptr[d.ptr + W + a]) + e0, static_cast<uint32_t>(nc * 4), bar);
+        for (int a = 0; a < 3; ++a)
+          bulk_load(sm_addr(stage + W * TmaCfg<W>::kRowBytes + a * TmaCfg<W>::kStateBytes + q0 * 4),
+                    static_cast<const float*>(p.ptr[d.ptr + W + a]) + e0 + q0, static_cast<uint32_t>(pe * 4), bar);
+      }
+    } else {
+#pragma unroll
+      for (int k = 0; k < W; ++k)
+        bulk_load(sm_addr(stage + k * TmaCfg<W>::kRowBytes), static_cast<const uint16_t*>(p.ptr[d.ptr + k]) + e0,
+                  static_cast<uint32_t>(nc * 2), bar);
+#pragma unroll
+      for (int a = 0; a < 3; ++a)
+        bulk_load(sm_addr(stage + W * TmaCfg<W>::kRowBytes + a * TmaCfg<W>::kStateBytes),
+                  static_cast<const float*>(p.ptr[d.ptr + W + a]) + e0, static_cast<uint32_t>(nc * 4), bar);
+    }
     return total;
   }
   if (d.kind == kCopy) {
@@ -227,7 +249,7 @@ __device__ __forceinline__ void tma_store_copy(const Params& p, const Seg& d, in
   bulk_wait_read_all();
 }
 
-template <int W>
+template <int W, bool kInterleave>
 __global__ void __launch_bounds__(kTmaThreads, 1) tma_kernel(const __grid_constant__ Params p) {
   extern __shared__ __align__(128) unsigned char smem[];
   __shared__ __align__(8) uint64_t full_bar[kTmaStages];
@@ -264,7 +286,7 @@ __global__ void __launch_bounds__(kTmaThreads, 1) tma_kernel(const __grid_consta
       const Seg& d = cur.at(p, c, l);
       const uint32_t extra = (blockIdx.x == 0 && i == 0) ? static_cast<uint32_t>(p.inject_tx) : 0u;
       const uint32_t bytes =
-          tma_chunk<W>(p, d, l, smem + stage * kStage, sm_addr(&full_bar[stage]), true, extra, &staged);
+          tma_chunk<W, kInterleave>(p, d, l, smem + stage * kStage, sm_addr(&full_bar[stage]), true, extra, &staged);
       if (bytes == 0) mbar_arrive(sm_addr(&full_bar[stage]));
       pending[stage] = static_cast<int>(round & 1u);
     }
@@ -288,7 +310,7 @@ __global__ void __launch_bounds__(kTmaThreads, 1) tma_kernel(const __grid_consta
     int64_t l, staged;
     const Seg& d = cur.at(p, c, l);
     const unsigned char* st = smem + stage * kStage;
-    const uint32_t bytes = tma_chunk<W>(p, d, l, const_cast<unsigned char*>(st), 0, false, 0u, &staged);
+    const uint32_t bytes = tma_chunk<W, kInterleave>(p, d, l, const_cast<unsigned char*>(st), 0, false, 0u, &staged);
     if (bytes != 0 && d.kind == kStep) {
       tma_consume_step<W>(p, d, l, st, staged);
     } else if (bytes != 0) {
