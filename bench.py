@@ -254,6 +254,65 @@ def build_sweep(n, W, torch, fs, synth):
 
 # ------------------------------------------------------------ the GPU arm
 
+def bench_line(info, workload_name, nproc, steps, warmup, ms_per_step, local_ms, launches_per_step,
+               tma_launches, l2_bytes, clocks, peak=None):
+    """The JSON line of the GPU arm. `ms_per_step`: the slowest rank's time per step;
+    `local_ms`: this rank's time for all `steps` (its launches' mean duration gives the
+    roofline's achieved bandwidth); `peak`: (GB/s, "measured"|"fallback"), read from
+    MEASURED_PEAKS.json when not given."""
+    bytes_step = info["bytes_per_step"]
+    value = whole_job_gbs(bytes_step, nproc, ms_per_step)
+    peak, peak_kind = measured_peaks() if peak is None else peak
+    mean_launch_ms = local_ms / (steps * launches_per_step)  # this rank's launches
+    achieved = bytes_step / launches_per_step / (mean_launch_ms * 1e-3) / 1e9
+    return {
+        "metric": METRIC,
+        "value": round(value, 2),
+        "unit": UNIT,
+        "n_gpus": nproc,
+        "steps": steps,
+        "warmup": warmup,
+        "ms_per_step": round(ms_per_step, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f32",
+        "data": "synthetic",
+        "config": {
+            "workload": workload_name,
+            "W": info["W"],
+            "units": info["units"],
+            "params": info["params"],
+            "elems_per_step": info["elems_per_step"],
+            "algorithmic_bytes_per_step": bytes_step,
+            "mode": info["mode"],
+            "parallelism": "W=%d virtual ranks in one GPU's HBM; %d GPU process(es), each an independent "
+                           "step, no data-path collective" % (info["W"], nproc),
+            "l2": ("inputs larger than L2: %.1f GB touched per step vs %.0f MB L2"
+                   % (bytes_step / 1e9, l2_bytes / 1e6) if bytes_step > 2 * l2_bytes else
+                   "working set %.0f MB is within 2x the %.0f MB L2: L2-resident, not an HBM figure"
+                   % (bytes_step / 1e6, l2_bytes / 1e6)),
+            "storage": "bf16 gradients/params, fp32 master/m/v",
+        },
+        "params_per_s": round(info["elems_per_step"] * nproc / (ms_per_step * 1e-3), 1),
+        "pct_of_hbm_peak": round(100.0 * value / nproc / peak, 2),
+        "pct_of_nominal_8tbs": round(100.0 * value / nproc / 8000.0, 2),
+        "roofline": {
+            "bound": "hbm",
+            "achieved": round(achieved, 2),
+            "peak": peak,
+            "unit": "GB/s",
+            "frac": round(achieved / peak, 4),
+            "peak_source": peak_kind,
+            "kernel": ("fsdp::tma_kernel<8>" if tma_launches == launches_per_step else
+                       "fsdp::segment_kernel<%d>" % (info["W"] if info["W"] in (1, 2, 4, 8, 16) else 0)),
+            "traffic": profiled_traffic(workload_name),
+        },
+        "gpu_launches": launches_per_step * steps,
+        "clocks": clocks,
+    }
+
+
 def run_ours(args):
     import torch
     import fully_sharded_gb300 as fs
@@ -335,60 +394,10 @@ def run_ours(args):
     total_ms = max_over_ranks(local_ms, dist)
     ms_per_step = total_ms / args.steps
     nproc = world
-    bytes_step = info["bytes_per_step"]
     # L2 size as the device reports it (129 MB on GB300 when the property is absent)
     l2 = float(getattr(torch.cuda.get_device_properties(local_rank), "L2_cache_size", 0) or 129e6)
-    value = whole_job_gbs(bytes_step, nproc, ms_per_step)
-    peak, peak_kind = measured_peaks()
-    mean_launch_ms = local_ms / (args.steps * launches_per_step)  # this rank's launches
-    achieved = bytes_step / launches_per_step / (mean_launch_ms * 1e-3) / 1e9
-    traffic = profiled_traffic(workload_name)
-    line = {
-        "metric": METRIC,
-        "value": round(value, 2),
-        "unit": UNIT,
-        "n_gpus": nproc,
-        "steps": args.steps,
-        "warmup": args.warmup,
-        "ms_per_step": round(ms_per_step, 4),
-        "higher_is_better": True,
-        "scaling": "weak",
-        "vs_baseline": None,
-        "dtype": "f32",
-        "data": "synthetic",
-        "config": {
-            "workload": workload_name,
-            "W": info["W"],
-            "units": info["units"],
-            "params": info["params"],
-            "elems_per_step": info["elems_per_step"],
-            "algorithmic_bytes_per_step": bytes_step,
-            "mode": info["mode"],
-            "parallelism": "W=%d virtual ranks in one GPU's HBM; %d GPU process(es), each an independent "
-                           "step, no data-path collective" % (info["W"], nproc),
-            "l2": ("inputs larger than L2: %.1f GB touched per step vs %.0f MB L2" % (bytes_step / 1e9, l2 / 1e6)
-                   if bytes_step > 2 * l2 else
-                   "working set %.0f MB is within 2x the %.0f MB L2: L2-resident, not an HBM figure"
-                   % (bytes_step / 1e6, l2 / 1e6)),
-            "storage": "bf16 gradients/params, fp32 master/m/v",
-        },
-        "params_per_s": round(info["elems_per_step"] * nproc / (ms_per_step * 1e-3), 1),
-        "pct_of_hbm_peak": round(100.0 * value / nproc / peak, 2),
-        "pct_of_nominal_8tbs": round(100.0 * value / nproc / 8000.0, 2),
-        "roofline": {
-            "bound": "hbm",
-            "achieved": round(achieved, 2),
-            "peak": peak,
-            "unit": "GB/s",
-            "frac": round(achieved / peak, 4),
-            "peak_source": peak_kind,
-            "kernel": ("fsdp::tma_kernel<8>" if tma_launches == launches_per_step else
-                       "fsdp::segment_kernel<%d>" % (info["W"] if info["W"] in (1, 2, 4, 8, 16) else 0)),
-            "traffic": traffic,
-        },
-        "gpu_launches": launches_per_step * args.steps,
-        "clocks": clk,
-    }
+    line = bench_line(info, workload_name, world, args.steps, args.warmup, ms_per_step, local_ms,
+                      launches_per_step, tma_launches, l2, clk)
     if not args.no_e2e and name == "llama7b" and not args.units:
         line["e2e"] = e2e_local_rank(args, torch, fs, synth, wls.LLAMA7B, units, info, bufs, rb, stream,
                                      nproc, dist)

@@ -48,3 +48,43 @@ def test_thread_results_equal_a_single_oracle_step():
 def test_cpu_model_is_named():
     name = bench.cpu_model()
     assert isinstance(name, str) and name
+
+
+def _info(W=8, elems=842301952, bytes_per_elem=70, units=33):
+    return dict(W=W, units=units, params=6738415616, elems_per_step=elems, bytes_per_step=bytes_per_elem * elems,
+                mode="local-rank", shard_elems=elems)
+
+
+def test_bench_line_carries_the_contract_keys_and_its_arithmetic():
+    info = _info()
+    clocks = {"sm_mhz": 2070.0, "sm_max_mhz": 2070.0, "reasons": [], "samples": 14}
+    line = bench.bench_line(info, "llama7b_local_rank", 1, 100, 5, 8.6, 860.0, 1, 1, 129e6, clocks,
+                            peak=(6786.2, "measured"))
+    for k in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better",
+              "scaling", "vs_baseline", "dtype", "data", "config", "roofline", "gpu_launches", "clocks"):
+        assert k in line, k
+    assert line["config"]["workload"] == "llama7b_local_rank"
+    assert line["higher_is_better"] is True and line["scaling"] == "weak" and line["vs_baseline"] is None
+    gbs = 70 * 842301952 / 8.6e-3 / 1e9
+    assert abs(line["value"] - gbs) < 0.01
+    r = line["roofline"]
+    assert set(r) >= {"bound", "achieved", "peak", "unit", "frac", "traffic"}
+    assert r["bound"] == "hbm" and r["unit"] == "GB/s" and r["peak"] == 6786.2
+    assert abs(r["achieved"] - gbs) < 0.01 and abs(r["frac"] - gbs / 6786.2) < 1e-4
+    assert r["kernel"] == "fsdp::tma_kernel<8>"
+    assert line["gpu_launches"] == 100 and line["clocks"] is clocks
+    assert "inputs larger than L2" in line["config"]["l2"]
+
+
+def test_bench_line_aggregates_ranks_and_names_the_ldg_form():
+    # two GPU processes, the slowest 10 ms per step; this rank's launches took 9 ms on average;
+    # two launches per step, none in the TMA form
+    info = _info(W=4, elems=10 ** 6, bytes_per_elem=2 * 4 + 26, units=1)
+    line = bench.bench_line(info, "sweep_1000000_W4", 2, 10, 3, 10.0, 180.0, 2, 0, 129e6, None,
+                            peak=(6800.0, "fallback"))
+    per_rank = 34 * 10 ** 6
+    assert abs(line["value"] - 2 * per_rank / 10e-3 / 1e9) < 0.01  # rounded to 2 decimals
+    assert abs(line["roofline"]["achieved"] - per_rank / 2 / 9e-3 / 1e9) < 0.01
+    assert line["roofline"]["kernel"] == "fsdp::segment_kernel<4>" and line["roofline"]["peak_source"] == "fallback"
+    assert line["gpu_launches"] == 20 and line["n_gpus"] == 2
+    assert "L2-resident" in line["config"]["l2"]
