@@ -88,3 +88,23 @@ def test_bench_line_aggregates_ranks_and_names_the_ldg_form():
     assert line["roofline"]["kernel"] == "fsdp::segment_kernel<4>" and line["roofline"]["peak_source"] == "fallback"
     assert line["gpu_launches"] == 20 and line["n_gpus"] == 2
     assert "L2-resident" in line["config"]["l2"]
+
+
+def test_reference_arm_prints_one_contract_line():
+    """`bench.py --impl reference` (the oracle on the host cores) runs without a GPU."""
+    import json
+    import os
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    out = subprocess.run([sys.executable, os.path.join(root, "bench.py"), "--impl", "reference", "--steps", "2",
+                          "--warmup", "3", "--ref-sample", "65536"], capture_output=True, text=True, timeout=300,
+                         cwd=root)
+    assert out.returncode == 0, out.stderr[-2000:]
+    lines = [l for l in out.stdout.splitlines() if l.strip()]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["unit"] == bench.UNIT and d["metric"] == bench.METRIC
+    assert d["config"]["workload"] == "llama7b_local_rank" and d["value"] > 0
+    assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["value"] == d["value"]
+    assert d["e2e"] == {"value": d["value"], "unit": d["unit"], "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
