@@ -94,8 +94,13 @@ extern "C" int fsdp_offload_step(const fsdp_offload_unit_t* units, int32_t n_uni
   const cudaStream_t compute = reinterpret_cast<cudaStream_t>(compute_s);
   const cudaStream_t h2d = reinterpret_cast<cudaStream_t>(h2d_s);
   const cudaStream_t d2h = reinterpret_cast<cudaStream_t>(d2h_s);
-  EventSet loaded(n_slots), stepped(n_slots), stored(n_slots), done(1);
-  if (!loaded.ok || !stepped.ok || !stored.ok || !done.ok) return FSDP_ECUDA;
+  EventSet loaded(n_slots), stepped(n_slots), stored(n_slots), start(1), done(1);
+  if (!loaded.ok || !stepped.ok || !stored.ok || !start.ok || !done.ok) return FSDP_ECUDA;
+  // the copies follow the work queued on `compute` before the call (the state's
+  // last use, and the steps of a previous call that used the slots)
+  if (cudaEventRecord(start.ev[0], compute) != cudaSuccess) return FSDP_ECUDA;
+  if (cudaStreamWaitEvent(h2d, start.ev[0], 0) != cudaSuccess) return FSDP_ECUDA;
+  if (cudaStreamWaitEvent(d2h, start.ev[0], 0) != cudaSuccess) return FSDP_ECUDA;
   std::vector<bool> used(n_slots, false);
   SegmentList list;
   for (int32_t i = 0; i < n_units; ++i) {
@@ -124,9 +129,9 @@ extern "C" int fsdp_offload_step(const fsdp_offload_unit_t* units, int32_t n_uni
     if (cudaEventRecord(stored.ev[slot], d2h) != cudaSuccess) return FSDP_ECUDA;
     used[slot] = true;
   }
-  // later work on any of the three streams follows every copy back
+  // `compute` follows every copy back (and, through the `loaded` events, every
+  // copy in): later work on `compute` sees the updated state in host memory
   if (cudaEventRecord(done.ev[0], d2h) != cudaSuccess) return FSDP_ECUDA;
   if (cudaStreamWaitEvent(compute, done.ev[0], 0) != cudaSuccess) return FSDP_ECUDA;
-  if (cudaStreamWaitEvent(h2d, done.ev[0], 0) != cudaSuccess) return FSDP_ECUDA;
   return FSDP_OK;
 }

@@ -87,8 +87,12 @@ int pipeline_step(const fsdp_pipeline_unit_t* units, int32_t n_units, int32_t ra
   const int W = n_units > 0 ? units[0].layout->world_size : 1;
   if (int rc = make_scalars(adam, W, &s)) return rc;
   if (n_units == 0) return FSDP_OK;
-  EventSet ready(n_slots), freed(n_slots), done(1);
-  if (!ready.ok || !freed.ok || !done.ok) return FSDP_ECUDA;
+  EventSet ready(n_slots), freed(n_slots), start(1);
+  if (!ready.ok || !freed.ok || !start.ok) return FSDP_ECUDA;
+  // the copies follow the work queued on `compute` before the call (its inputs,
+  // and the steps of a previous call that read the staging slots)
+  if (cudaEventRecord(start.ev[0], compute) != cudaSuccess) return FSDP_ECUDA;
+  if (cudaStreamWaitEvent(copy, start.ev[0], 0) != cudaSuccess) return FSDP_ECUDA;
   std::vector<bool> used(n_slots, false);
   SegmentList list;
   for (int32_t i = 0; i < n_units; ++i) {
@@ -114,9 +118,8 @@ int pipeline_step(const fsdp_pipeline_unit_t* units, int32_t n_units, int32_t ra
         cudaMemcpyAsync(u.shard_out, u.full_out + rank * S, S * 2, cudaMemcpyDefault, compute) != cudaSuccess)
       return FSDP_ECUDA;
   }
-  // later work on `copy` (e.g. the next call's first refill) follows this call's steps
-  if (cudaEventRecord(done.ev[0], compute) != cudaSuccess) return FSDP_ECUDA;
-  if (cudaStreamWaitEvent(copy, done.ev[0], 0) != cudaSuccess) return FSDP_ECUDA;
+  // every copy of the call was waited for by `compute` (the `ready` events), so
+  // `compute` is now ordered after all of the call's work on both streams
   return FSDP_OK;
 }
 

@@ -266,9 +266,12 @@ int fsdp_selftest_wait_timeout(const void *src, void *dst, int64_t bytes, int64_
  * slot_numel >= padded_numel of every unit (its W x S slices); n_slots in
  * [1, 8]; its contents are overwritten. The pool's size is the transient
  * gradient budget: 2 * n_slots * slot_numel bytes.
- * When the call returns, `copy` is ordered after every operation it queued on
- * `compute`, so later work on either stream sees the results. The two streams
- * may be the same stream (no overlap). Results are bit-identical to
+ * The call's copies start after the work queued on `compute` before the call
+ * (so inputs written there, and a previous call's steps, come first); when the
+ * call returns, `compute` is ordered after everything the call queued on both
+ * streams, so later work on `compute` sees the results (order later work on
+ * `copy` after `compute` yourself). The two streams may be the same stream (no
+ * overlap). The call can be captured into a CUDA graph from `compute`. Results are bit-identical to
  * fsdp_shard_step_grouped on the same values. EINVAL: F != W, a unit with
  * another W, bad rank, n_slots outside [1,8], a slot too small, null pointers;
  * EALIAS: outputs overlapping inputs, the staging pool or each other. */
@@ -314,9 +317,11 @@ int fsdp_pipeline_step(const fsdp_pipeline_unit_t *units, int32_t n_units, int32
  * of 4 keeps every slot array 16-byte aligned, the vector path). n_slots in
  * [1, 8]. master/exp_avg/exp_avg_sq: host memory, page-locked for the copies
  * to overlap (pageable memory works but each copy then waits for the host);
- * device memory also works. When the call returns, `compute` and `h2d` are
- * ordered after the last copy back, so later work on any of the three streams
- * sees the updated state. The streams may coincide (no overlap). Results are
+ * device memory also works. The call's copies start after the work queued
+ * on `compute` before the call; when the call returns, `compute` is ordered
+ * after everything the call queued, the last copy back included, so later work
+ * on `compute` sees the updated state. The streams may coincide (no overlap).
+ * The call can be captured into a CUDA graph from `compute`. Results are
  * bit-identical to fsdp_shard_step_grouped with the same state in HBM.
  * EINVAL: F != W, a unit with another W, bad rank, n_slots outside [1,8], a
  * slot too small, null pointers; EALIAS: outputs (state, full_out, staging)
