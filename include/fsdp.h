@@ -28,9 +28,11 @@
  * Conventions for every call:
  *   - The caller owns all memory. The library allocates nothing and keeps no
  *     state about the data between calls (it caches the SM count and kernel
- *     occupancy per device; fsdp_pipeline_step creates and releases CUDA
- *     events within a call; fsdp_pipeline_step_noalloc stages through a fixed
- *     array that is part of the library's device code, see there).
+ *     occupancy per device; fsdp_pipeline_step and fsdp_offload_step create
+ *     and release CUDA events within a call; fsdp_pipeline_step_noalloc stages
+ *     through a fixed array that is part of the library's device code, see
+ *     there; a per-device status word records a device wait that ran out, see
+ *     fsdp_device_status).
  *   - "device" pointers point to CUDA global memory of the current device;
  *     pointer arrays themselves (const T* const*) are HOST arrays of device
  *     pointers and are read before the call returns.
@@ -40,7 +42,8 @@
  *     page-locked host memory mapped into the device's address space
  *     (cudaHostAlloc, or cudaHostRegister with cudaHostRegisterMapped, at an
  *     address the device can use as is). The kernels then read and write the
- *     state over the host link; nothing else changes.
+ *     state over the host link; nothing else changes. fsdp_offload_step
+ *     instead copies the state between host memory and device slots.
  *   - bf16 values are passed as their uint16_t bit patterns; fp32 as float.
  *   - Every GPU call is asynchronous on `stream` (0 = legacy default stream).
  *     Inputs must stay unchanged, and outputs untouched, until the stream has
@@ -69,7 +72,7 @@ typedef struct CUstream_st *fsdp_stream_t;
                             rank outside [0,W), inconsistent layout, step < 1,
                             weight_decay != 0, ... */
 #define FSDP_EALIAS (-2) /* an output overlaps an input or another output */
-#define FSDP_ECUDA (-3)  /* a CUDA launch failed (cudaGetLastError) */
+#define FSDP_ECUDA (-3)  /* a CUDA call or launch failed (cudaGetLastError) */
 #define FSDP_ENOSPACE (-4) /* the work does not fit the fixed staging capacity of
                               fsdp_pipeline_step_noalloc */
 
@@ -222,9 +225,10 @@ int fsdp_shard_step_grouped_launches(const fsdp_unit_args_t *units, int32_t n_un
 
 /* As fsdp_shard_step_grouped_launches, and *tma_launches_out (if not NULL)
  * receives how many of those launches use the TMA form of the kernel (bulk
- * copies into a shared-memory pipeline; chosen for W = 8 launches with one
- * replica per position and enough chunks to fill every SM's pipeline). Needs
- * no GPU, but reads the SM count of the current device when one is present. */
+ * copies into a shared-memory pipeline; chosen for W = 8 launches made of
+ * one-replica step segments, and copies, with enough chunks to fill every SM's
+ * pipeline). Needs no GPU, but reads the SM count of the current device when
+ * one is present. */
 int fsdp_shard_step_grouped_plan(const fsdp_unit_args_t *units, int32_t n_units,
                                  int32_t rank_begin, int32_t rank_end, int32_t *launches_out,
                                  int32_t *tma_launches_out);
