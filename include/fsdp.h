@@ -275,8 +275,9 @@ int fsdp_selftest_wait_timeout(const void *src, void *dst, int64_t bytes, int64_
  * call returns, `compute` is ordered after everything the call queued on both
  * streams, so later work on `compute` sees the results (order later work on
  * `copy` after `compute` yourself). The two streams may be the same stream (no
- * overlap). The call can be captured into a CUDA graph from `compute`. Results are bit-identical to
- * fsdp_shard_step_grouped on the same values. EINVAL: F != W, a unit with
+ * overlap). The call can be captured into a CUDA graph from `compute`.
+ * Results are bit-identical to fsdp_shard_step_grouped on the same values.
+ * EINVAL: F != W, a unit with
  * another W, bad rank, n_slots outside [1,8], a slot too small, null pointers;
  * EALIAS: outputs overlapping inputs, the staging pool or each other. */
 typedef struct {
