@@ -919,6 +919,10 @@ def main():
     args = ap.parse_args()
     if args.warmup < 3:
         raise SystemExit("at least 3 warm-up steps")
+    _, world, _ = env_rank()
+    if args.gpus != world:
+        raise SystemExit("--gpus %d but %d process(es): run N > 1 GPUs as python -m torch.distributed.run "
+                         "--nproc-per-node N bench.py --gpus N" % (args.gpus, world))
     if args.impl == "reference":
         run_reference(args)
     elif args.workload == "pipeline":

@@ -108,3 +108,13 @@ def test_reference_arm_prints_one_contract_line():
     assert d["config"]["workload"] == "llama7b_local_rank" and d["value"] > 0
     assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["value"] == d["value"]
     assert d["e2e"] == {"value": d["value"], "unit": d["unit"], "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
+
+
+def test_bench_refuses_a_gpu_count_it_was_not_launched_with():
+    import os
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    out = subprocess.run([sys.executable, os.path.join(root, "bench.py"), "--gpus", "2"], capture_output=True,
+                         text=True, timeout=120, cwd=root)
+    assert out.returncode != 0 and "nproc-per-node" in out.stderr
