@@ -227,6 +227,24 @@ def pin_adam_torch(ora, seed=5):
         assert _close(p, tp) and _close(m, tm) and _close(v, tv), (gscale, t0, nonzero)
 
 
+def pin_adam_torch_hyper(ora, seed=12):
+    """Against torch.optim.Adam at large step counters (bias corrections near 1, where a
+    wrong power of beta still shows) and with other hyper-parameters."""
+    rng = np.random.default_rng(seed)
+    n = 4096
+    other = dict(lr=1e-2, beta1=0.8, beta2=0.95, eps=1e-6)
+    for hp, t0 in ((ADAM, 1000), (ADAM, 1_000_000), (other, 1), (other, 50), (other, 20_000)):
+        p0 = (rng.standard_normal(n) * 0.02).astype(np.float32)
+        m0 = (rng.standard_normal(n) * 1e-4).astype(np.float32)
+        v0 = (np.abs(rng.standard_normal(n)) * 1e-4).astype(np.float32)
+        grads = [(rng.standard_normal(n) * 1e-3).astype(np.float32) for _ in range(3)]
+        tp, tm, tv = _torch_adam_steps(p0, m0, v0, grads, t0, hp)
+        p, m, v = p0.copy(), m0.copy(), v0.copy()
+        for k, g in enumerate(grads):
+            ora.adam(p, m, v, g, step=t0 + k, **hp)
+        assert _close(p, tp) and _close(m, tm) and _close(v, tv), (hp, t0)
+
+
 def pin_adam_first_step(ora, seed=6):
     """From m = v = 0 at t = 1: mhat = g and vhat = g^2, so p' = p - lr g / (|g| + eps)."""
     rng = np.random.default_rng(seed)
@@ -497,5 +515,5 @@ ALL_PINS = [
     pin_adam_torch, pin_adam_first_step, pin_adam_zero_grad,
     pin_cast_torch,
     pin_step_ddp_torch, pin_step_f_continuum, pin_step_local_rank,
-    pin_account_worked_example, pin_account_ring, pin_account_zero,
+    pin_account_worked_example, pin_account_ring, pin_account_zero, pin_adam_torch_hyper,
 ]
