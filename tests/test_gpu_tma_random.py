@@ -128,3 +128,43 @@ def test_random_tma_launch(ora, seed):
                 gu.assert_same_bits(_gather(unit["full_out"][0], k * S + jk), want, "gathered unit %d k %d" % (u, k))
     del units, bufs
     torch.cuda.empty_cache()
+
+
+def test_grouped_launch_split_over_both_forms(ora):
+    """45 local-rank units of 4 M elements: the grouped step needs two descriptor tables
+    (40 units of 8 segments each fit one); the first holds enough chunks for the TMA form,
+    the second (5 units) runs on the LDG form. Every unit's sampled outputs match."""
+    torch = gu.torch()
+    rng = np.random.default_rng(990)
+    sizes = [4_000_000 + int(rng.integers(0, 64)) for _ in range(45)]  # odd sizes: mixed alignment
+    wl = wls.Workload("tma_split", 7, [[(P,)] for P in sizes], W, sigma_state=1e-4)
+    rank, step = 5, 77
+    units, info, bufs = bench.build_local_rank(wl, rank, torch, fs, synth)
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    launches, tma = fs.fsdp_shard_step_grouped_plan(units, rank, rank + 1)
+    assert launches == 2
+    if sms <= 152:
+        assert tma == 1
+    fs.fsdp_shard_step_grouped(units, rank, rank + 1, gu.adam_hyper(step))
+    torch.cuda.synchronize()
+    for u in (0, 1, 39, 40, 44):  # both sides of the split
+        unit = units[u]
+        S, P = unit["layout"].shard_numel, unit["layout"].numel
+        j = _positions(S, rng)
+        i = rank * S + j
+        rows = [synth.normal_bf16_at(wls.key_grad(wl, u % 2, k, 0), i, wl.sigma_grad) for k in range(W)]
+        master = synth.normal_f32_at(wls.key_master(wl, u), i, wl.sigma_master, n_valid=P)
+        m = synth.normal_f32_at(wls.key_exp_avg(wl, u), i, wl.sigma_state, absval=True, n_valid=P)
+        v = synth.normal_f32_at(wls.key_exp_avg_sq(wl, u), i, wl.sigma_state, absval=True, n_valid=P)
+        g = ora.fold_mean(rows)
+        op, om, ov = master.copy(), m.copy(), v.copy()
+        obf = ora.adam(op, om, ov, g, step=step, **gu.HP)
+        gu.assert_same_bits(_gather(unit["master"][0], j), op, "master unit %d" % u)
+        gu.assert_same_bits(_gather(unit["exp_avg"][0], j), om, "exp_avg unit %d" % u)
+        gu.assert_same_bits(_gather(unit["exp_avg_sq"][0], j), ov, "exp_avg_sq unit %d" % u)
+        gu.assert_same_bits(_gather(unit["full_out"][0], i), obf, "bf16 unit %d" % u)
+        jk = _positions(S, rng, k=24)
+        want = synth.normal_bf16_at(wls.key_shard(wl, u), 0 * S + jk, wl.sigma_master, n_valid=P)
+        gu.assert_same_bits(_gather(unit["full_out"][0], jk), want, "gathered unit %d" % u)
+    del units, bufs
+    torch.cuda.empty_cache()
