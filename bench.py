@@ -148,14 +148,16 @@ class ClockSampler:
 
 # --------------------------------------------------------------- workloads
 
-def build_local_rank(wl, rank, torch, fs, synth):
-    """Device buffers of one rank's step over all units (local-rank mode)."""
+def build_local_rank(wl, rank, torch, fs, synth, row_numel=0):
+    """Device buffers of one rank's step over all units (local-rank mode). `row_numel`:
+    the length of each gradient row of the pool (at least the largest unit's padded
+    size, which is the default)."""
     from synth import workloads as wls
     W = wl.world_size
     lays = [fs.fsdp_flatten_layout(wls.numels(u), W)[0] for u in wl.units]
     S_tot = sum(l.shard_numel for l in lays)
     pad_tot = sum(l.padded_numel for l in lays)
-    maxpad = max(l.padded_numel for l in lays)
+    maxpad = max([l.padded_numel for l in lays] + [row_numel])
     dev = torch.device("cuda")
     # gradient pool: 2 unit-sets of W rows (units alternate between them)
     slots = min(2, len(lays))
@@ -328,11 +330,15 @@ def run_ours(args):
     name = args.workload
     if name == "llama7b":
         wl = wls.LLAMA7B
+        row_numel = 0
         if args.units:
+            # the first units, with the gradient rows as far apart as in the whole step
+            row_numel = max(fs.fsdp_flatten_layout(wls.numels(u), wl.world_size)[0].padded_numel
+                            for u in wl.units)
             wl = wls.Workload(wl.name, wl.config_id, wl.units[:args.units], wl.world_size,
                               sigma_state=wl.sigma_state)
         vrank = virtual_rank(rank, wl.world_size)
-        units, info, bufs = build_local_rank(wl, vrank, torch, fs, synth)
+        units, info, bufs = build_local_rank(wl, vrank, torch, fs, synth, row_numel)
         rb, re = vrank, vrank + 1
         workload_name = "llama7b_local_rank" + ("_units%d" % args.units if args.units else "")
     elif name in ("llama_block", "gpt2_small", "tiny_mlp"):
@@ -909,7 +915,7 @@ def main():
     ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", default="llama7b")
-    ap.add_argument("--units", type=int, default=0, help="llama7b: only the first N units")
+    ap.add_argument("--units", type=int, default=0, help="llama7b: only the first N units (gradient rows spaced as in the whole step)")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=10)

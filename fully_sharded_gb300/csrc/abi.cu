@@ -159,15 +159,19 @@ bool use_tma(const Params& p, int tma_grid) {
   return step && p.total_chunks >= static_cast<int64_t>(kTmaMinChunksPerBlock) * tma_grid;
 }
 
-// A TMA launch whose step segments have gradient rows spanning 4 GiB or more
+// A TMA launch whose step segments have gradient rows spanning 3 GiB or more
 // of addresses stages them in interleaved quarter-chunk copies (the second
-// instantiation of the kernel). Measured on GB300 (interleaved A/B): with 8
-// rows 1 GB apart (a 5e8-element FlatParameter, 7 GB span) and 2 GB apart (1e9
-// elements, 14 GB span), one 4 KB copy per row ran 2.1-3.1 % slower than
-// interleaved 1 KB pieces, likely DRAM bank mapping; with spans up to 3.7 GB
-// (GPT-2, the Llama block, the 7B units) interleaving gained nothing, and on
-// GPT-2 its four times as many copies cost 2 %.
-constexpr uintptr_t kInterleaveSpread = uintptr_t(4) << 30;
+// instantiation of the kernel). Measured on GB300 (interleaved A/B, W = 8,
+// every launch forced to one form or the other): one FlatParameter of 2.5e8
+// to 1e9 elements (rows 0.5 to 2 GB apart, spans 3.3 to 13 GiB) ran 2.5-3.1 %
+// faster with interleaved 1 KB pieces than with one 4 KB copy per row, likely
+// DRAM bank mapping, and the 7B local-rank step (rows 0.52 GB apart, 3.4 GiB)
+// 0.1-0.5 %; GPT-2 small (13 units, spans near 0.1 GiB) ran 2 % slower with
+// four times as many copies, a 5e7-element FlatParameter 1.4 % and the Llama
+// block (2.6 GiB) 1 % slower on one box of three. Below 3 GiB the results
+// are mixed (a 2e8-element FlatParameter, 2.6 GiB, gained 2.5 %), so the rule
+// keeps the one-copy form there.
+constexpr uintptr_t kInterleaveSpread = uintptr_t(3) << 30;
 
 bool wants_interleave(const Params& p) {
   for (int k = 0; k < p.nseg; ++k) {

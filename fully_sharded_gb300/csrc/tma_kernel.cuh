@@ -12,7 +12,7 @@
 //
 // Two instantiations: kInterleave = false stages a step chunk with one bulk
 // copy per array; kInterleave = true (the host picks it when a launch's
-// gradient rows span 4 GiB or more of addresses) in four rounds of quarter
+// gradient rows span 3 GiB or more of addresses) in four rounds of quarter
 // chunks over the arrays.
 //
 // Measured on GB300 against segment_kernel (same chunks, same arithmetic,

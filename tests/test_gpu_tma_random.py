@@ -9,6 +9,8 @@ library to choose the TMA form (checked with the plan). Inputs are filled on
 the device by the seeded generator; the host regenerates them at sampled
 positions (the ends of every shard, chunk boundaries, random positions), the
 oracle computes those outputs, and they must equal the device's bit for bit.
+Two more local-rank cases space the gradient rows widely enough for the
+library to pick the interleaved-copy staging.
 """
 import numpy as np
 import pytest
@@ -71,9 +73,20 @@ def _draw_units(rng, local, need_chunks):
 
 @pytest.mark.parametrize("seed", range(6))
 def test_random_tma_launch(ora, seed):
+    _check_random_launch(ora, seed, seed % 2 == 0)
+
+
+@pytest.mark.parametrize("seed", (6, 7))
+def test_random_tma_launch_wide_rows(ora, seed):
+    """Local-rank launches whose gradient rows sit 2^28 elements apart (a 3.5 GiB span
+    over the eight rows): the library stages their step chunks in interleaved
+    quarter-chunk copies, the form the 7B step runs."""
+    _check_random_launch(ora, seed, True, row_numel=1 << 28)
+
+
+def _check_random_launch(ora, seed, local, row_numel=0):
     torch = gu.torch()
     rng = np.random.default_rng(900 + seed)
-    local = seed % 2 == 0
     sms = torch.cuda.get_device_properties(0).multi_processor_count
     wl = wls.Workload("tma_random_%d" % seed, 7, _draw_units(rng, local, 130 * sms), W, sigma_state=1e-4)
     hp = dict(lr=float(10 ** rng.uniform(-4, -2)), beta1=float(rng.uniform(0.8, 0.95)),
@@ -81,7 +94,7 @@ def test_random_tma_launch(ora, seed):
     step = int(rng.integers(1, 5000))
     rank = int(rng.integers(0, W))
     if local:
-        units, info, bufs = bench.build_local_rank(wl, rank, torch, fs, synth)
+        units, info, bufs = bench.build_local_rank(wl, rank, torch, fs, synth, row_numel)
         rb, re = rank, rank + 1
     else:
         units, info, bufs = bench.build_all_ranks(wl, W, torch, fs, synth)
