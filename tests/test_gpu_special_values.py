@@ -1,6 +1,9 @@
 """Special values through the fused step: +-inf, NaN, subnormal and signed-zero gradients,
 huge and subnormal parameters. Non-NaN outputs must equal the oracle bit for bit; NaN must
-appear exactly where the oracle has NaN (NaN payloads are not specified)."""
+appear exactly where the oracle has NaN (NaN payloads are not specified). The first case
+runs on the LDG form (W = 4, one small unit); the others put the same kind of unit at W = 8
+into a grouped launch with a zero-filled unit large enough for the library to choose the
+TMA form, all ranks and one rank with its gather."""
 import numpy as np
 import pytest
 
@@ -75,3 +78,88 @@ def test_special_values_match_oracle(ora):
         nan_seen += int(np.isnan(om[r]).sum())
     _same_or_both_nan_bf16(gu.to_host(full), ofull[0], "full")
     assert nan_seen > 0  # the case does reach the NaN paths
+
+
+def _special_inputs(rng, W, P, padded):
+    """Host inputs of one unit: W bf16 gradient rows and fp32 master/m/v over the padded
+    FlatParameter (the pad stays zero), sprinkled with special values."""
+    specials = np.array([np.inf, -np.inf, np.nan, 0.0, -0.0, 1e-40, -1e-40, 3.3e38, -3.3e38, 1e-3],
+                        dtype=np.float32)
+    grads = []
+    for k in range(W):
+        x = np.zeros(padded, np.float32)
+        x[:P] = rng.standard_normal(P) * 1e-2
+        idx = rng.choice(P, size=P // 16, replace=False)
+        x[idx] = rng.choice(specials, size=idx.size)
+        grads.append(_bf16(x))
+    master = np.zeros(padded, np.float32)
+    master[:P] = rng.standard_normal(P) * 0.02
+    idx = rng.choice(P, size=P // 16, replace=False)
+    master[idx] = rng.choice(np.array([0.0, -0.0, 1e-40, 3e38, -3e38, 1.0], np.float32), size=idx.size)
+    m = np.zeros(padded, np.float32)
+    v = np.zeros(padded, np.float32)
+    m[:P] = np.abs(rng.standard_normal(P) * 1e-4)
+    v[:P] = np.abs(rng.standard_normal(P) * 1e-4)
+    v[rng.choice(P, size=P // 32, replace=False)] = 0.0
+    return grads, master, m, v
+
+
+def _filler_unit(torch, W, owned, chunks_needed, local):
+    """A zero-filled unit whose chunks bring the launch to the TMA form's threshold."""
+    if local:  # a step chunk of 2048 elements plus W - 1 gather chunks of 16 KB per 8192 elements
+        S = 8192 * -(-chunks_needed // (4 + W - 1))
+    else:
+        S = 2048 * -(-chunks_needed // W)
+    lay, _ = fs.fsdp_flatten_layout([W * S], W)
+    z = lambda n, dt: torch.zeros(n, dtype=dt, device="cuda")  # noqa: E731
+    return dict(layout=lay, grads=[z(W * S, torch.int16) for _ in range(W)],
+                master=[z(S, torch.float32) for _ in owned], exp_avg=[z(S, torch.float32) for _ in owned],
+                exp_avg_sq=[z(S, torch.float32) for _ in owned],
+                other_shards=[None if k in owned else z(S, torch.int16) for k in range(W)] if local else None,
+                full_out=[z(W * S, torch.int16)])
+
+
+@pytest.mark.parametrize("local", [False, True])
+def test_special_values_tma_form(ora, local):
+    torch = gu.torch()
+    W, P = 8, 8 * 8192 - 3  # shards of 8192 elements (16-byte aligned), a ragged last shard
+    lay, _ = fs.fsdp_flatten_layout([P], W)
+    S, padded = lay.shard_numel, lay.padded_numel
+    grads, master, m, v = _special_inputs(np.random.default_rng(40 + local), W, P, padded)
+    rank = 5
+    owned = [rank] if local else list(range(W))
+    others = [gu.host_normal(synth.stream_key(78, 5), S, 0.02, idx0=k * S, bf16=True) for k in range(W)]
+    om = [master[r * S:(r + 1) * S].copy() for r in owned]
+    oe = [m[r * S:(r + 1) * S].copy() for r in owned]
+    ov = [v[r * S:(r + 1) * S].copy() for r in owned]
+    ofull = [np.zeros(padded, np.uint16)]
+    ora.shard_step(grads, W, owned[0], owned[-1] + 1, om, oe, ov, others if local else None, ofull,
+                   step=3, **gu.HP)
+    unit = dict(layout=lay, grads=[gu.to_dev(g) for g in grads],
+                master=[gu.to_dev(master[r * S:(r + 1) * S]) for r in owned],
+                exp_avg=[gu.to_dev(m[r * S:(r + 1) * S]) for r in owned],
+                exp_avg_sq=[gu.to_dev(v[r * S:(r + 1) * S]) for r in owned],
+                other_shards=[None if k in owned else gu.to_dev(others[k]) for k in range(W)] if local else None,
+                full_out=[torch.zeros(padded, dtype=torch.int16, device="cuda")])
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    units = [unit, _filler_unit(torch, W, owned, 130 * sms, local)]
+    launches, tma = fs.fsdp_shard_step_grouped_plan(units, owned[0], owned[-1] + 1)
+    assert (launches, tma) == (1, 1), (launches, tma)
+    fs.fsdp_shard_step_grouped(units, owned[0], owned[-1] + 1, gu.adam_hyper(3))
+    torch.cuda.synchronize()
+    nan_seen = 0
+    for i, r in enumerate(owned):
+        _same_or_both_nan(gu.to_host(unit["master"][i]), om[i], "master r%d" % r)
+        _same_or_both_nan(gu.to_host(unit["exp_avg"][i]), oe[i], "exp_avg r%d" % r)
+        _same_or_both_nan(gu.to_host(unit["exp_avg_sq"][i]), ov[i], "exp_avg_sq r%d" % r)
+        nan_seen += int(np.isnan(om[i]).sum())
+    got = gu.to_host(unit["full_out"][0])
+    if local:  # the gathered shards are byte copies: compare every element, NaN or not
+        for k in range(W):
+            if k != rank:
+                gu.assert_same_bits(got[k * S:(k + 1) * S], ofull[0][k * S:(k + 1) * S], "gathered k%d" % k)
+        got, want = got[rank * S:(rank + 1) * S], ofull[0][rank * S:(rank + 1) * S]
+    else:
+        want = ofull[0]
+    _same_or_both_nan_bf16(got, want, "full")
+    assert nan_seen > 0
