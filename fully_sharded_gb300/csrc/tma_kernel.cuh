@@ -19,8 +19,9 @@
 // bit-identical results): W = 8 single-replica step launches gain 1-4 %
 // (Llama block 1.246 -> 1.206 ms); W <= 4, replica-heavy hybrid steps, short
 // launches and launches of reduce chunks lose, so the host uses this form only
-// for W = 8 launches made of one-replica step segments (and copies) with at
-// least kTmaMinChunksPerBlock chunks per block.
+// for W = 8 launches made of one-replica step segments (and copies), and for
+// launches of copies only (and zero fills: pack, unpack, the gathers; 1-3.5 %
+// faster), with at least kTmaMinChunksPerBlock chunks per block.
 //
 // Every mbarrier wait is bounded in time (Params::wait_limit_ns, read from
 // %globaltimer): when a wait runs out the block sets bit 0 of g_fsdp_status,
