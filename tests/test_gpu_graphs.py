@@ -1,6 +1,11 @@
-"""The library's launches inside CUDA graphs: a grouped step (the TMA form) and a
-pipelined step over two streams are captured once and replayed; every replay
-equals the same call made directly, bit for bit."""
+"""The library's launches inside CUDA graphs: a grouped step (the TMA form), a
+pipelined step over two streams and a staged offload step over three are captured
+once and replayed; every replay equals the same call made directly, bit for bit.
+The last cases capture the first library call of a fresh process."""
+import os
+import subprocess
+import sys
+
 import pytest
 
 import gpu_util as gu
@@ -113,3 +118,57 @@ def test_staged_offload_replays_from_a_graph():
         assert torch.equal(direct[1][n].view(torch.int32), graphed[1][n].view(torch.int32)), n
     for u, v in zip(direct[0], graphed[0]):
         assert torch.equal(u["full_out"][0], v["full_out"][0])
+
+
+_FIRST_CALL = r"""
+import sys
+import torch
+sys.path[:0] = [sys.argv[1], sys.argv[2]]
+import bench, fully_sharded_gb300 as fs, gpu_util as gu, synth
+torch.cuda.set_device(0)
+case = sys.argv[3]
+W = 8 if case in ("tma", "pipeline") else 4
+s = torch.cuda.Stream()
+g = torch.cuda.CUDAGraph()
+if case == "pipeline":
+    wl = bench.sweep_workload(W * 300_000 + 3, W)
+    sets = []
+    for _ in range(2):
+        units, info, bufs = bench.build_local_rank(wl, 2, torch, fs, synth)
+        sets.append((units, bench.pipeline_setup(torch, fs, units, info, 2, 2)))
+    (u1, (b1, st1, sl1, k1)), (u2, (b2, st2, sl2, k2)) = sets
+    copy = torch.cuda.Stream()
+    with torch.cuda.graph(g, stream=s):
+        fs.fsdp_pipeline_step(b2, 2, st2, sl2, 2, gu.adam_hyper(5), compute=torch.cuda.current_stream(), copy=copy)
+    g.replay()
+    fs.fsdp_pipeline_step(b1, 2, st1, sl1, 2, gu.adam_hyper(5), compute=s, copy=copy)
+    pairs = [(a[n][0], b[n][0]) for a, b in zip(u1, u2) for n in ("master", "exp_avg", "exp_avg_sq", "full_out")]
+else:
+    wl = bench.sweep_workload(40_000_000 if case == "tma" else 4_000_003, W)
+    direct = bench.build_all_ranks(wl, W, torch, fs, synth)[0]
+    graphed = bench.build_all_ranks(wl, W, torch, fs, synth)[0]
+    batch = fs.UnitBatch(graphed)
+    with torch.cuda.graph(g, stream=s):
+        fs.fsdp_shard_step_grouped(batch, 0, W, gu.adam_hyper(3), stream=torch.cuda.current_stream())
+    g.replay()
+    fs.fsdp_shard_step_grouped(direct, 0, W, gu.adam_hyper(3), stream=s)
+    pairs = [(a[n][i], b[n][i]) for a, b in zip(direct, graphed)
+             for n in ("master", "exp_avg", "exp_avg_sq", "full_out") for i in range(len(a[n]))]
+torch.cuda.synchronize()
+assert all(torch.equal(x.view(torch.int8), y.view(torch.int8)) for x, y in pairs)
+code = fs.fsdp_device_status()
+assert code == 0, code
+print("same bits")
+"""
+
+
+@pytest.mark.parametrize("case", ["tma", "ldg", "pipeline"])
+def test_first_call_of_a_process_inside_a_capture(case):
+    """A fresh process whose first library call is made while a stream is being captured
+    (the per-device sizing queries then run inside the capture): the replay equals the
+    same call made directly, bit for bit. One process per case, so nothing is cached."""
+    here = os.path.dirname(os.path.abspath(__file__))
+    root = os.path.dirname(here)
+    r = subprocess.run([sys.executable, "-c", _FIRST_CALL, root, here, case], capture_output=True, text=True,
+                       timeout=600, cwd=root)
+    assert r.returncode == 0 and "same bits" in r.stdout, r.stdout[-2000:] + r.stderr[-4000:]
