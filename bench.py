@@ -506,6 +506,28 @@ def host_link(torch, stream, nbytes=1 << 31, reps=3):
     return out
 
 
+def host_link_both_ways(torch, h2d, d2h, nbytes=3 << 30, reps=3):
+    """Pinned host <-> device copy bandwidth with both directions at once (GB/s summed over
+    the two), best of `reps`: one copy of `nbytes` each way, on two streams."""
+    hs = torch.empty(nbytes // 2, dtype=torch.int16, pin_memory=True)
+    hs.zero_()
+    hd = torch.empty(nbytes // 2, dtype=torch.int16, pin_memory=True)
+    ds = torch.zeros(nbytes // 2, dtype=torch.int16, device="cuda")
+    dd = torch.empty(nbytes // 2, dtype=torch.int16, device="cuda")
+    best = float("inf")
+    for _ in range(reps):
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        with torch.cuda.stream(h2d):
+            dd.copy_(hs, non_blocking=True)
+        with torch.cuda.stream(d2h):
+            hd.copy_(ds, non_blocking=True)
+        torch.cuda.synchronize()
+        best = min(best, time.perf_counter() - t0)
+    del hs, hd, ds, dd
+    return round(2 * nbytes / best / 1e9, 1)
+
+
 def run_unfused(args):
     """The step's parts as separate calls, timed on the Llama block (W = 8, all ranks):
     per rank fsdp_reduce_scatter (fp32 gradient shard out) and fsdp_adam_shard_step
@@ -644,6 +666,9 @@ def run_offload(args):
             "staging_bytes": staging.numel() * 4}
         del staging
     best = min(v["ms_per_step"] for v in staged.values())
+    # the staged step moves 12 B per shard element each way, both directions at once
+    both = host_link_both_ways(torch, h2d, d2h)
+    floor_ms = 12 * S_tot / (both / 2 * 1e9) * 1e3
     print(json.dumps({
         "workload": "llama7b_local_rank_state_offload", "W": wl.world_size, "shard_elems": S_tot,
         "state_in_hbm": {"ms_per_step": round(ms_hbm, 3),
@@ -653,6 +678,8 @@ def run_offload(args):
                                  "host_link_bytes_per_step": 24 * S_tot,
                                  "host_link_GB_per_s": round(24 * S_tot / (ms_host * 1e-3) / 1e9, 1)},
         "state_in_host_memory_staged": staged,
+        "host_link_both_ways": {"GB_per_s_total": both, "floor_ms": round(floor_ms, 2),
+                                "staged_frac_of_floor": round(floor_ms / best, 4)},
         "gpu_memory_saved_bytes": 12 * S_tot,
         "slowdown": round(ms_host / ms_hbm, 2),
         "staged_slowdown": round(best / ms_hbm, 2),
