@@ -408,8 +408,11 @@ def run_ours(args):
         line["e2e"] = e2e_local_rank(args, torch, fs, synth, wls.LLAMA7B, units, info, bufs, rb, stream,
                                      nproc, dist)
     # the oracle baseline: rank 0 of a one-GPU run only
-    if world == 1 and rank == 0 and not args.no_cpu_baseline and name == "llama7b":
-        line["cpu_baseline"] = cpu_baseline(units, info, bufs, rb, torch, seconds=args.cpu_seconds)
+    if world == 1 and rank == 0 and not args.no_cpu_baseline:
+        if name == "llama7b":
+            line["cpu_baseline"] = cpu_baseline(units, info, bufs, rb, torch, seconds=args.cpu_seconds)
+        else:
+            line["cpu_baseline"] = cpu_baseline_all_ranks(units, torch, seconds=min(args.cpu_seconds, 3.0))
     if dist:
         dist.destroy_process_group()
     if rank == 0:
@@ -473,6 +476,16 @@ def e2e_local_rank(args, torch, fs, synth, wl, units, info, bufs, rank, stream, 
     k = max(1, min(args.steps, args.e2e_steps))
     copy = torch.cuda.Stream()
     ms = time_pipeline(torch, fs, batch, staging, slot, 2, rank, k, args.warmup, dist, stream, copy)
+    # the same steps once more, each timed on its own (synchronized before and after):
+    # steps far above the median are the host link busy with work outside this process
+    per_step = []
+    for i in range(k):
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        fs.fsdp_pipeline_step(batch, rank, staging, slot, 2, fs.AdamHyper(step=20_000 + i), compute=stream,
+                              copy=copy)
+        torch.cuda.synchronize()
+        per_step.append((time.perf_counter() - t0) * 1e3)
     h2d_bytes = 2 * W * S_tot
     link = host_link(torch, copy)
     floor_ms = h2d_bytes / (link["h2d_GB_per_s"] * 1e9) * 1e3
@@ -480,9 +493,11 @@ def e2e_local_rank(args, torch, fs, synth, wl, units, info, bufs, rank, stream, 
     return {"value": round(whole_job_gbs(info["bytes_per_step"], nproc, ms), 2), "unit": UNIT,
             "h2d_bytes_per_step": h2d_bytes, "d2h_bytes_per_step": 2 * S_tot, "ms_per_step": round(ms, 3),
             "steps": k, "host_link": link,
+            "per_step_ms": {"median": round(statistics.median(per_step), 2), "min": round(min(per_step), 2),
+                            "max": round(max(per_step), 2)},
             "note": "host wall clock around K fsdp_pipeline_step calls (2 staging slots), pinned host "
-                    "buffers; host_link: pinned copy bandwidth measured right after, floor_ms = the "
-                    "step's H2D bytes at that rate"}
+                    "buffers; per_step_ms: K more calls, each timed alone; host_link: pinned copy "
+                    "bandwidth measured right after, floor_ms = the step's H2D bytes at that rate"}
 
 
 def host_link(torch, stream, nbytes=1 << 31, reps=3):
@@ -831,6 +846,51 @@ def cpu_baseline(units, info, bufs, rank, torch, seconds=10.0, n_s=1 << 22):
            "cpu": cpu_model()}
     out["all_cores"] = cpu_baseline_all_cores(ora, grads, master, m, v, others, rank, n_s, per, seconds)
     return out
+
+
+def oracle_sample_all_ranks(units, n_s):
+    """Unit 0 of an all-ranks workload (any F) cut to the first n_s elements of every
+    position's shard: a unit of padded length F * n_s with the same W, F and work per
+    element, copied to the host (gradient rows, every rank's state)."""
+    import numpy as np
+    u = units[0]
+    lay = u["layout"]
+    W, F, S = lay.world_size, lay.shard_factor, lay.shard_numel
+    n_s = max(1, min(n_s, S))
+    grads = np.empty((W, F * n_s), np.uint16)
+    for k in range(W):
+        row = u["grads"][k]
+        for p in range(F):
+            grads[k, p * n_s:(p + 1) * n_s] = row[p * S:p * S + n_s].cpu().numpy().view(np.uint16)
+    state = [[t[:n_s].cpu().numpy().copy() for t in u[name]] for name in ("master", "exp_avg", "exp_avg_sq")]
+    return grads, state, W, F, n_s
+
+
+def cpu_baseline_all_ranks(units, torch, seconds=3.0, elems=1 << 20):
+    """The oracle on one core, timed on a sample of unit 0 of an all-ranks (or hybrid) workload:
+    about `elems` padded elements; GB/s at the workload's algorithmic bytes per element."""
+    import numpy as np
+    import oracle
+    ora = oracle.load()
+    F = units[0]["layout"].shard_factor
+    grads, (master, m, v), W, F, n_s = oracle_sample_all_ranks(units, max(1, elems // F))
+    R = W // F
+    per = (2 * W + 26 * R) * F * n_s
+    full = [np.zeros(F * n_s, np.uint16) for _ in range(R)]
+    t0 = time.perf_counter()
+    reps = 0
+    while True:
+        ora.shard_step(list(grads), F, 0, W, master, m, v, None, full, lr=1e-3, beta1=0.9, beta2=0.999,
+                       eps=1e-8, step=reps + 1)
+        reps += 1
+        if time.perf_counter() - t0 >= seconds:
+            break
+    dt = time.perf_counter() - t0
+    return {"value": round(per * reps / dt / 1e9, 4), "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": "unit 0 of the workload cut to the first %d elements of every position's shard "
+                      "(W=%d, F=%d: %d padded elements), every rank stepped, %d repetitions in %.1f s; "
+                      "same algorithmic bytes per element" % (n_s, W, F, F * n_s, reps, dt),
+            "cpu": cpu_model()}
 
 
 def host_cores():

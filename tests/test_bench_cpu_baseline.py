@@ -45,6 +45,46 @@ def test_thread_results_equal_a_single_oracle_step():
     assert not np.array_equal(a[0], master)
 
 
+def _hybrid_units(W=8, F=4, P=8 * 1000 + 3, seed=0):
+    import torch
+    import fully_sharded_gb300 as fs
+    lay, _ = fs.fsdp_flatten_layout([P], W, F)
+    S, padded, R = lay.shard_numel, lay.padded_numel, W // F
+    gen = torch.Generator().manual_seed(seed)
+    g = (torch.randn((W, padded), generator=gen) * 1e-3).to(torch.bfloat16).view(torch.int16)
+    st = [torch.randn((R, padded), generator=gen).abs() * 1e-4 for _ in range(3)]
+    view = lambda a, r: a[r // F, (r % F) * S:(r % F + 1) * S]  # noqa: E731
+    return [dict(layout=lay, grads=[g[k] for k in range(W)], master=[view(st[0], r) for r in range(W)],
+                 exp_avg=[view(st[1], r) for r in range(W)], exp_avg_sq=[view(st[2], r) for r in range(W)],
+                 other_shards=None, full_out=[torch.zeros(padded, dtype=torch.int16) for _ in range(R)])], g, st
+
+
+def test_all_ranks_sample_takes_the_head_of_every_position():
+    units, g, st = _hybrid_units()
+    lay = units[0]["layout"]
+    S = lay.shard_numel
+    grads, (master, m, v), W, F, n_s = bench.oracle_sample_all_ranks(units, 100)
+    assert (W, F, n_s) == (8, 4, 100) and grads.shape == (8, 400)
+    gn = g.numpy().view(np.uint16)
+    for k in range(W):
+        for p in range(F):
+            assert np.array_equal(grads[k, p * 100:(p + 1) * 100], gn[k, p * S:p * S + 100])
+    for r in range(W):
+        assert np.array_equal(master[r], st[0][r // F, (r % F) * S:(r % F) * S + 100].numpy())
+        assert np.array_equal(v[r], st[2][r // F, (r % F) * S:(r % F) * S + 100].numpy())
+
+
+def test_all_ranks_baseline_times_the_oracle_and_leaves_the_units_unchanged():
+    import torch
+    units, g, st = _hybrid_units(seed=1)
+    before = [t.clone() for t in st]
+    res = bench.cpu_baseline_all_ranks(units, torch, seconds=0.2, elems=4096)
+    assert res["value"] > 0 and res["unit"] == bench.UNIT and res["cores"] == 1 and res["kind"] == "oracle"
+    assert "F=4" in res["sample"]
+    for a, b in zip(st, before):
+        assert torch.equal(a, b)
+
+
 def test_cpu_model_is_named():
     name = bench.cpu_model()
     assert isinstance(name, str) and name

@@ -1,0 +1,42 @@
+"""The bench's end-to-end measurement (the pipelined call with host buffers) on a small
+local-rank workload: the keys of its record, the bytes it counts per step, and the
+per-step distribution it reports beside the block-timed value."""
+import argparse
+
+import pytest
+
+import gpu_util as gu
+import synth
+
+pytestmark = pytest.mark.gpu
+
+fs = pytest.importorskip("fully_sharded_gb300")
+bench = pytest.importorskip("bench")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _cuda():
+    torch = pytest.importorskip("torch")
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA GPU")
+
+
+def test_e2e_record():
+    torch = gu.torch()
+    wl = bench.sweep_workload(8 * 1_000_000 + 5, 8)
+    rank = 3
+    units, info, bufs = bench.build_local_rank(wl, rank, torch, fs, synth)
+    args = argparse.Namespace(steps=4, e2e_steps=4, warmup=2)
+    stream = torch.cuda.Stream()
+    e = bench.e2e_local_rank(args, torch, fs, synth, wl, units, info, bufs, rank, stream, 1, None)
+    S_tot = info["shard_elems"]
+    assert e["unit"] == bench.UNIT and e["value"] > 0 and e["steps"] == 4
+    assert e["h2d_bytes_per_step"] == 2 * 8 * S_tot and e["d2h_bytes_per_step"] == 2 * S_tot
+    # value: the algorithmic bytes of one step over the block-timed step time
+    assert abs(e["value"] - info["bytes_per_step"] / (e["ms_per_step"] * 1e-3) / 1e9) <= 0.01 * e["value"] + 0.05
+    p = e["per_step_ms"]
+    assert 0 < p["min"] <= p["median"] <= p["max"]
+    link = e["host_link"]
+    assert link["h2d_GB_per_s"] > 0 and link["d2h_GB_per_s"] > 0
+    assert abs(link["floor_ms"] - e["h2d_bytes_per_step"] / (link["h2d_GB_per_s"] * 1e9) * 1e3) < 0.02
+    assert fs.fsdp_device_status() == 0
