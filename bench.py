@@ -486,18 +486,26 @@ def e2e_local_rank(args, torch, fs, synth, wl, units, info, bufs, rank, stream, 
                               copy=copy)
         torch.cuda.synchronize()
         per_step.append((time.perf_counter() - t0) * 1e3)
-    h2d_bytes = 2 * W * S_tot
+    h2d_bytes, d2h_bytes = 2 * W * S_tot, 2 * S_tot
     link = host_link(torch, copy)
     floor_ms = h2d_bytes / (link["h2d_GB_per_s"] * 1e9) * 1e3
-    link.update({"floor_ms": round(floor_ms, 2), "frac_of_floor": round(floor_ms / ms, 4)})
+    # the results go back while inputs still come in: during those bytes each direction
+    # runs at the two-way rate, the rest of the inputs at the one-way rate
+    both = host_link_both_ways(torch, copy, torch.cuda.Stream())
+    floor2_ms = (d2h_bytes / (both / 2 * 1e9) + (h2d_bytes - d2h_bytes) / (link["h2d_GB_per_s"] * 1e9)) * 1e3
+    link.update({"floor_ms": round(floor_ms, 2), "frac_of_floor": round(floor_ms / ms, 4),
+                 "both_ways_GB_per_s_total": both, "floor_two_way_ms": round(floor2_ms, 2),
+                 "frac_of_floor_two_way": round(floor2_ms / ms, 4)})
     return {"value": round(whole_job_gbs(info["bytes_per_step"], nproc, ms), 2), "unit": UNIT,
-            "h2d_bytes_per_step": h2d_bytes, "d2h_bytes_per_step": 2 * S_tot, "ms_per_step": round(ms, 3),
+            "h2d_bytes_per_step": h2d_bytes, "d2h_bytes_per_step": d2h_bytes, "ms_per_step": round(ms, 3),
             "steps": k, "host_link": link,
             "per_step_ms": {"median": round(statistics.median(per_step), 2), "min": round(min(per_step), 2),
                             "max": round(max(per_step), 2)},
             "note": "host wall clock around K fsdp_pipeline_step calls (2 staging slots), pinned host "
                     "buffers; per_step_ms: K more calls, each timed alone; host_link: pinned copy "
-                    "bandwidth measured right after, floor_ms = the step's H2D bytes at that rate"}
+                    "bandwidth measured right after, floor_ms = the step's H2D bytes at the one-way "
+                    "rate, floor_two_way_ms = its D2H bytes at the two-way rate (both directions "
+                    "loaded) plus the remaining H2D bytes at the one-way rate"}
 
 
 def host_link(torch, stream, nbytes=1 << 31, reps=3):
@@ -785,7 +793,12 @@ def run_pipeline(args):
         torch.cuda.empty_cache()
     base = res["prefetch_0"]["ms_per_step"]
     link = host_link(torch, copy)
-    link["floor_ms"] = round(2 * wl.world_size * info["shard_elems"] / (link["h2d_GB_per_s"] * 1e9) * 1e3, 2)
+    h2d_bytes, d2h_bytes = 2 * wl.world_size * info["shard_elems"], 2 * info["shard_elems"]
+    link["floor_ms"] = round(h2d_bytes / (link["h2d_GB_per_s"] * 1e9) * 1e3, 2)
+    both = host_link_both_ways(torch, copy, compute)
+    link["both_ways_GB_per_s_total"] = both
+    link["floor_two_way_ms"] = round((d2h_bytes / (both / 2 * 1e9) + (h2d_bytes - d2h_bytes)
+                                      / (link["h2d_GB_per_s"] * 1e9)) * 1e3, 2)
     print(json.dumps({"workload": "llama7b_local_rank_pipeline", "W": wl.world_size, "rank": vrank,
                       "host_link": link,
                       "units": info["units"], "largest_unit_params": U,

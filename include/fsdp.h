@@ -266,6 +266,12 @@ int fsdp_selftest_wait_timeout(const void *src, void *dst, int64_t bytes, int64_
  *                 then copy the new bf16 shard to shard_out if given.
  * With n_slots = 1 (prefetch 0) copies and steps alternate; with n_slots = 2
  * (prefetch 1) the copy of unit u+1 overlaps the step of unit u.
+ * The first and the last unit go through the same cycle in pieces of at most
+ * 4,194,304 shard elements (whole 2048-element chunks; one 2D copy of the W
+ * slices' ranges, one step and one shard_out copy per piece; each piece takes
+ * the next slot), so that the first step starts before a whole unit has
+ * arrived and little remains after the last copy in. Results do not depend on
+ * the pieces.
  * staging: device bf16 buffer of n_slots x slot_numel elements, caller-owned,
  * slot_numel >= padded_numel of every unit (its W x S slices); n_slots in
  * [1, 8]; its contents are overwritten. The pool's size is the transient

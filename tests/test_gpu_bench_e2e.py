@@ -39,4 +39,8 @@ def test_e2e_record():
     link = e["host_link"]
     assert link["h2d_GB_per_s"] > 0 and link["d2h_GB_per_s"] > 0
     assert abs(link["floor_ms"] - e["h2d_bytes_per_step"] / (link["h2d_GB_per_s"] * 1e9) * 1e3) < 0.02
+    r_both = link["both_ways_GB_per_s_total"] / 2 * 1e9
+    floor2 = (e["d2h_bytes_per_step"] / r_both
+              + (e["h2d_bytes_per_step"] - e["d2h_bytes_per_step"]) / (link["h2d_GB_per_s"] * 1e9)) * 1e3
+    assert abs(link["floor_two_way_ms"] - floor2) < 0.02
     assert fs.fsdp_device_status() == 0

@@ -123,3 +123,48 @@ def test_pipeline_equals_grouped_step():
     for u, gr in zip(units, grouped):
         assert torch.equal(u["master"], gr["master"][0]) and torch.equal(u["full_out"], gr["full_out"][0])
         assert torch.equal(u["exp_avg"], gr["exp_avg"][0]) and torch.equal(u["exp_avg_sq"], gr["exp_avg_sq"][0])
+
+
+def _bf16_bits(x):
+    return (np.asarray(x, np.float32).view(np.uint32) >> 16).astype(np.uint16)
+
+
+def test_edge_units_in_pieces_match_oracle(ora):
+    """First and last units above 4 M shard elements (odd lengths: ragged last pieces, an
+    odd own-slice offset), a short unit between them: the pipeline moves the edge units in
+    pieces; every output equals the oracle's local-rank step of each unit bit for bit."""
+    torch = gu.torch()
+    rng = np.random.default_rng(7700)
+    sizes = [8 * (4194304 + 6149), 8 * 100000 + 5, 8 * (4194304 + 2 * 2048 + 3)]
+    units, host = [], []
+    for P in sizes:
+        lay, _ = fs.fsdp_flatten_layout([P], W)
+        S, padded = lay.shard_numel, lay.padded_numel
+        valid = max(0, min(S, P - RANK * S))
+        master = np.zeros(S, np.float32)
+        master[:valid] = rng.standard_normal(valid) * 0.02
+        m = np.abs(rng.standard_normal(S)).astype(np.float32) * 1e-4
+        v = np.abs(rng.standard_normal(S)).astype(np.float32) * 1e-4
+        others = [_bf16_bits(rng.standard_normal(S) * 0.02) for _ in range(W)]
+        slices = np.stack([_bf16_bits(rng.standard_normal(S) * 1e-2) for _ in range(W)])
+        units.append(dict(layout=lay, master=gu.to_dev(master), exp_avg=gu.to_dev(m), exp_avg_sq=gu.to_dev(v),
+                          other_shards=[None if j == RANK else gu.to_dev(others[j]) for j in range(W)],
+                          full_out=torch.zeros(padded, dtype=torch.int16, device="cuda"),
+                          shard_out=torch.zeros(S, dtype=torch.int16).pin_memory(),
+                          grad_slices=torch.from_numpy(slices.view(np.int16).copy()).pin_memory()))
+        host.append(dict(lay=lay, master=master, m=m, v=v, others=others, slices=slices))
+    slot = max(u["layout"].padded_numel for u in units)
+    staging = torch.empty(2 * slot, dtype=torch.int16, device="cuda")
+    fs.fsdp_pipeline_step(units, RANK, staging, slot, 2, gu.adam_hyper(4), compute=torch.cuda.Stream(),
+                          copy=torch.cuda.Stream())
+    torch.cuda.synchronize()
+    for i, (u, h) in enumerate(zip(units, host)):
+        want_full = oracle_step(ora, h, h["slices"], 4)
+        S = h["lay"].shard_numel
+        gu.assert_same_bits(gu.to_host(u["master"]), h["master"], "master unit %d" % i)
+        gu.assert_same_bits(gu.to_host(u["exp_avg"]), h["m"], "exp_avg unit %d" % i)
+        gu.assert_same_bits(gu.to_host(u["exp_avg_sq"]), h["v"], "exp_avg_sq unit %d" % i)
+        gu.assert_same_bits(gu.to_host(u["full_out"]), want_full, "full unit %d" % i)
+        gu.assert_same_bits(u["shard_out"].numpy().view(np.uint16), want_full[RANK * S:(RANK + 1) * S],
+                            "shard_out unit %d" % i)
+    assert fs.fsdp_device_status() == 0
