@@ -105,6 +105,30 @@ def test_gpt2_small_grouped(ora):
     del units, keep
 
 
+@pytest.mark.parametrize("W", [2, 4, 8, 16])
+def test_sweep_1e9_all_ranks(ora, W):
+    """One FlatParameter of 1e9 elements stepped for all W ranks, as the size sweep times it:
+    the LDG form at W = 2, 4, 16 and the TMA form with interleaved copies at W = 8 (rows 2 GB
+    apart). Sampled outputs of every rank, plus positions around each 2 GiB boundary of the
+    flat fp32 state, equal the oracle's."""
+    torch = gu.torch()
+    n = 1_000_000_000
+    wl = bench.sweep_workload(n, W)
+    units, info, keep = bench.build_all_ranks(wl, W, torch, fs, synth)
+    launches, tma = fs.fsdp_shard_step_grouped_plan(units, 0, W)
+    assert launches == 1 and tma == (1 if W == 8 else 0)
+    fs.fsdp_shard_step_grouped(units, 0, W, gu.adam_hyper(2))
+    torch.cuda.synchronize()
+    padded = units[0]["layout"].padded_numel
+    # every rank's fp32 state is a view of one flat array: flat index x is at byte 4x,
+    # so these positions sit on each 2 GiB boundary of it
+    edges = [k << 29 for k in range(1, (padded >> 29) + 1) if (k << 29) < padded]
+    check_all_ranks_unit(ora, wl, 0, units[0], W, None, 2, seed=40 + W, extra_global=edges)
+    assert fs.fsdp_device_status() == 0
+    del units, keep
+    torch.cuda.empty_cache()
+
+
 def test_hybrid_full_size_identical_across_F(ora):
     torch = gu.torch()
     wl = wls.HYBRID
