@@ -489,13 +489,14 @@ def e2e_local_rank(args, torch, fs, synth, wl, units, info, bufs, rank, stream, 
     h2d_bytes, d2h_bytes = 2 * W * S_tot, 2 * S_tot
     link = host_link(torch, copy)
     floor_ms = h2d_bytes / (link["h2d_GB_per_s"] * 1e9) * 1e3
-    # the results go back while inputs still come in: during those bytes each direction
-    # runs at the two-way rate, the rest of the inputs at the one-way rate
-    both = host_link_both_ways(torch, copy, torch.cuda.Stream())
-    floor2_ms = (d2h_bytes / (both / 2 * 1e9) + (h2d_bytes - d2h_bytes) / (link["h2d_GB_per_s"] * 1e9)) * 1e3
-    link.update({"floor_ms": round(floor_ms, 2), "frac_of_floor": round(floor_ms / ms, 4),
-                 "both_ways_GB_per_s_total": both, "floor_two_way_ms": round(floor2_ms, 2),
-                 "frac_of_floor_two_way": round(floor2_ms / ms, 4)})
+    link.update({"floor_ms": round(floor_ms, 2), "frac_of_floor": round(floor_ms / ms, 4)})
+    if nproc == 1:  # one process: the host's link and memory are not shared with other ranks
+        # the results go back while inputs still come in: during those bytes each direction
+        # runs at the two-way rate, the rest of the inputs at the one-way rate
+        both = host_link_both_ways(torch, copy, torch.cuda.Stream())
+        floor2_ms = (d2h_bytes / (both / 2 * 1e9) + (h2d_bytes - d2h_bytes) / (link["h2d_GB_per_s"] * 1e9)) * 1e3
+        link.update({"both_ways_GB_per_s_total": both, "floor_two_way_ms": round(floor2_ms, 2),
+                     "frac_of_floor_two_way": round(floor2_ms / ms, 4)})
     return {"value": round(whole_job_gbs(info["bytes_per_step"], nproc, ms), 2), "unit": UNIT,
             "h2d_bytes_per_step": h2d_bytes, "d2h_bytes_per_step": d2h_bytes, "ms_per_step": round(ms, 3),
             "steps": k, "host_link": link,
