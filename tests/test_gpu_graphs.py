@@ -59,11 +59,13 @@ def test_grouped_step_replays_from_a_graph():
         assert torch.equal(a.view(torch.int8), b.view(torch.int8))
 
 
-def test_pipelined_step_replays_from_a_graph():
-    """Copies on one stream, steps on another, ordered by events: captured as one graph."""
+@pytest.mark.parametrize("shard", [300_000, 4_300_000])
+def test_pipelined_step_replays_from_a_graph(shard):
+    """Copies on one stream, steps on another, ordered by events: captured as one graph
+    (a unit of 4.3 M shard elements moves in pieces, with 2D copies)."""
     torch = gu.torch()
     _warm(torch)
-    wl = bench.sweep_workload(8 * 300_000 + 3, 8)
+    wl = bench.sweep_workload(8 * shard + 3, 8)
     units, info, bufs = bench.build_local_rank(wl, 2, torch, fs, synth)
     units2, _, _ = bench.build_local_rank(wl, 2, torch, fs, synth)
     batch, staging, slot, keep = bench.pipeline_setup(torch, fs, units, info, 2, 2)
