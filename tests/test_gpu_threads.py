@@ -1,7 +1,8 @@
 """Host-side thread safety of the library: several threads drive it at once, each
-on its own stream and buffers (the LDG form, a hybrid launch and the TMA form),
-while another thread calls the host-only entry points. Every result must equal
-the same calls made one after another, bit for bit."""
+on its own stream and buffers (the LDG form, a hybrid launch and the TMA form;
+then the pipelined and offload schedulers and copy-only launches), while another
+thread calls the host-only entry points. Every result must equal the same calls
+made one after another, bit for bit."""
 import threading
 
 import pytest
@@ -91,3 +92,95 @@ def test_concurrent_threads_match_sequential_calls():
     for (a, _, _), (b, _, _), c in zip(seq, thr, CASES):
         for x, y in zip(_outputs(a), _outputs(b)):
             assert torch.equal(x.view(torch.int8), y.view(torch.int8)), "case %r" % (c,)
+
+
+def _pipeline_set(torch, shard):
+    wl = bench.sweep_workload(8 * shard + 3, 8)
+    units, info, bufs = bench.build_local_rank(wl, 2, torch, fs, synth)
+    batch, staging, slot, keep = bench.pipeline_setup(torch, fs, units, info, 2, 2)
+    return units, batch, staging, slot, keep
+
+
+def _offload_set(torch, shard):
+    wl = bench.sweep_workload(8 * shard + 5, 8)
+    units, info, bufs = bench.build_local_rank(wl, 1, torch, fs, synth)
+    host = {n: bufs[n].cpu().pin_memory() for n in ("master", "exp_avg", "exp_avg_sq")}
+    off, so = [], 0
+    for u in units:
+        S = u["layout"].shard_numel
+        off.append(dict(layout=u["layout"], grads=u["grads"], master=host["master"][so:so + S],
+                        exp_avg=host["exp_avg"][so:so + S], exp_avg_sq=host["exp_avg_sq"][so:so + S],
+                        other_shards=u["other_shards"], full_out=u["full_out"][0]))
+        so += S
+    slot = (max(u["layout"].shard_numel for u in units) + 3) // 4 * 4
+    return units, host, fs.OffloadBatch(off), torch.empty(3 * 3 * slot, device="cuda"), slot
+
+
+def test_concurrent_schedulers_match_sequential_calls():
+    """A pipelined step (its unit moving in pieces), a staged offload step and copy-only
+    TMA-form launches (pack) from three threads at once, each with its own streams and
+    buffers, equal the same calls made one after another."""
+    torch = gu.torch()
+    sets = []
+    for _ in range(2):  # [0]: one after another, [1]: all at once
+        pipe = _pipeline_set(torch, 4_300_000)
+        off = _offload_set(torch, 1_000_000)
+        numels = [45_000_001, 3, 45_000_005]  # 22,000 copy chunks: the TMA form on 152 SMs
+        lay, offs = fs.fsdp_flatten_layout(numels, 8)
+        tens = [torch.randn(n, device="cuda", generator=torch.Generator("cuda").manual_seed(i)) for i, n in
+                enumerate(numels)]
+        flat = torch.empty(lay.padded_numel, device="cuda")
+        sets.append((pipe, off, (tens, lay, offs, flat)))
+    torch.cuda.synchronize()
+    streams = [[torch.cuda.Stream() for _ in range(3)] for _ in range(3)]
+
+    def run_pipe(s, st):
+        units, batch, staging, slot, keep = s
+        for t in range(1, 4):
+            fs.fsdp_pipeline_step(batch, 2, staging, slot, 2, gu.adam_hyper(t), compute=st[0], copy=st[1])
+        st[0].synchronize()
+
+    def run_off(s, st):
+        units, host, batch, staging, slot = s
+        for t in range(1, 4):
+            fs.fsdp_offload_step(batch, 1, staging, slot, 3, gu.adam_hyper(t), compute=st[0], h2d=st[1], d2h=st[2])
+        st[0].synchronize()
+
+    def run_pack(s, st):
+        tens, lay, offs, flat = s
+        for _ in range(3):
+            fs.fsdp_pack_flat(tens, lay, offs, flat, stream=st[0])
+        st[0].synchronize()
+
+    runs = (run_pipe, run_off, run_pack)
+    for k, fn in enumerate(runs):
+        fn(sets[0][k], streams[k])
+    start = threading.Barrier(3)
+    errors = []
+
+    def worker(k):
+        try:
+            torch.cuda.set_device(0)
+            start.wait()
+            runs[k](sets[1][k], streams[k])
+        except Exception as e:  # reported below, on the main thread
+            errors.append(e)
+
+    threads = [threading.Thread(target=worker, args=(k,)) for k in range(3)]
+    for t in threads:
+        t.start()
+    for t in threads:
+        t.join()
+    assert not errors, errors
+    torch.cuda.synchronize()
+    (pa, oa, ka), (pb, ob, kb) = sets
+    for u, v in zip(pa[0], pb[0]):
+        for name in ("master", "exp_avg", "exp_avg_sq", "full_out"):
+            assert torch.equal(u[name][0].view(torch.int8), v[name][0].view(torch.int8)), "pipeline " + name
+    assert torch.equal(pa[4][1], pb[4][1]), "pipeline shard_out"
+    for n in ("master", "exp_avg", "exp_avg_sq"):
+        assert torch.equal(oa[1][n].view(torch.int32), ob[1][n].view(torch.int32)), "offload " + n
+    for u, v in zip(oa[0], ob[0]):
+        assert torch.equal(u["full_out"][0], v["full_out"][0]), "offload full_out"
+    assert torch.equal(ka[3].view(torch.int32), kb[3].view(torch.int32)), "pack"
+    assert fs.fsdp_device_status() == 0
