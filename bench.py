@@ -62,6 +62,18 @@ def max_over_ranks(x: float, dist) -> float:
     return float(t.item())
 
 
+def all_ranks_ok(ok: bool, dist) -> bool:
+    """True when every rank reports ok (no-op without a process group): ranks agree before a
+    step that would otherwise leave a failed rank out of the next collective."""
+    if dist is None or not dist.is_initialized() or dist.get_world_size() == 1:
+        return bool(ok)
+    import torch
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([1 if ok else 0], dtype=torch.int32, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MIN)
+    return bool(t.item())
+
+
 def whole_job_gbs(bytes_per_step_per_rank: int, nproc: int, ms_per_step: float) -> float:
     """Aggregate algorithmic GB/s: every rank's bytes over the slowest rank's step time."""
     return bytes_per_step_per_rank * nproc / (ms_per_step * 1e-3) / 1e9
@@ -472,7 +484,17 @@ def e2e_local_rank(args, torch, fs, synth, wl, units, info, bufs, rank, stream, 
     step (prefetch 1)."""
     W = info["W"]
     S_tot = info["shard_elems"]
-    batch, staging, slot, keep = pipeline_setup(torch, fs, units, info, rank, 2)
+    # the inputs' page-locked host buffers (2 W + 2 bytes per shard element per rank): every
+    # rank must have them before any rank enters the timed, synchronised steps
+    err = None
+    try:
+        batch, staging, slot, keep = pipeline_setup(torch, fs, units, info, rank, 2)
+    except (RuntimeError, MemoryError) as e:
+        err = str(e).splitlines()[0][:160] if str(e) else type(e).__name__
+    if not all_ranks_ok(err is None, dist):
+        return {"value": None, "unit": UNIT, "h2d_bytes_per_step": 2 * W * S_tot, "d2h_bytes_per_step": 2 * S_tot,
+                "unavailable": "page-locked host buffers for the step's inputs could not be allocated on every "
+                               "rank" + (": " + err if err else "")}
     k = max(1, min(args.steps, args.e2e_steps))
     copy = torch.cuda.Stream()
     ms = time_pipeline(torch, fs, batch, staging, slot, 2, rank, k, args.warmup, dist, stream, copy)

@@ -27,7 +27,8 @@ def _worker(rank, world, port, out):
     local_ms = 10.0 + 5.0 * rank
     slowest = bench.max_over_ranks(local_ms, dist)
     value = bench.whole_job_gbs(70 * 842301952, w, slowest)
-    out.put((r, w, lr, bench.virtual_rank(r, 8), slowest, value))
+    agree = (bench.all_ranks_ok(True, dist), bench.all_ranks_ok(rank != 1, dist))
+    out.put((r, w, lr, bench.virtual_rank(r, 8), slowest, value, agree))
     dist.barrier()
     dist.destroy_process_group()
 
@@ -48,10 +49,13 @@ def test_two_ranks_take_the_slowest_time_and_aggregate_bytes():
     assert all(x[4] == 15.0 for x in res)
     want = 70 * 842301952 * 2 / 15e-3 / 1e9
     assert all(x[5] == pytest.approx(want) for x in res)
+    # every rank learns that one rank failed (no rank proceeds alone into a collective)
+    assert all(x[6] == (True, False) for x in res)
 
 
 def test_single_process_is_a_no_op():
     assert bench.max_over_ranks(3.5, None) == 3.5
+    assert bench.all_ranks_ok(True, None) and not bench.all_ranks_ok(False, None)
     assert bench.virtual_rank(9, 8) == 1
 
 
