@@ -34,6 +34,7 @@ def test_e2e_record():
     assert e["h2d_bytes_per_step"] == 2 * 8 * S_tot and e["d2h_bytes_per_step"] == 2 * S_tot
     # value: the algorithmic bytes of one step over the block-timed step time
     assert abs(e["value"] - info["bytes_per_step"] / (e["ms_per_step"] * 1e-3) / 1e9) <= 0.01 * e["value"] + 0.05
+    assert len(e["blocks_ms"]) == 3 and abs(min(e["blocks_ms"]) - e["ms_per_step"]) < 0.002
     p = e["per_step_ms"]
     assert 0 < p["min"] <= p["median"] <= p["max"]
     link = e["host_link"]
