@@ -631,6 +631,7 @@ def run_unfused(args):
     peak, _ = measured_peaks()
     row = lambda ms, b: {"ms": round(ms, 4), "GB_per_s": round(b / (ms * 1e-3) / 1e9, 1),  # noqa
                          "frac_of_peak": round(b / (ms * 1e-3) / 1e9 / peak, 4)}
+    base = None if args.no_cpu_baseline else oracle_parts_baseline(W, 1 << 17)
     print(json.dumps({
         "workload": "llama_block_all_ranks_unfused", "W": W, "padded_elems": padded,
         "reduce_scatter_x8": row(t_rs, b_rs), "adam_shard_step_x8": row(t_ad, b_ad), "all_gather": row(t_ag, b_ag),
@@ -638,7 +639,7 @@ def run_unfused(args):
         "fused": row(t_fused, (2 * W + 26) * padded),
         "fused_speedup": round((t_rs + t_ad + t_ag) / t_fused, 3),
         "pack_f32": row(t_pack, 8 * lay2.numel),
-        "bytes_per_element": {"unfused": 2 * W + 38, "fused": 2 * W + 26}}), flush=True)
+        "bytes_per_element": {"unfused": 2 * W + 38, "fused": 2 * W + 26}, "cpu_baseline": base}), flush=True)
 
 
 def run_offload(args):
@@ -720,8 +721,10 @@ def run_offload(args):
     # the staged step moves 12 B per shard element each way, both directions at once
     both = host_link_both_ways(torch, h2d, d2h)
     floor_ms = 12 * S_tot / (both / 2 * 1e9) * 1e3
+    base = None if args.no_cpu_baseline else cpu_baseline(units, info, bufs, 0, torch, seconds=3.0)
     print(json.dumps({
         "workload": "llama7b_local_rank_state_offload", "W": wl.world_size, "shard_elems": S_tot,
+        "cpu_baseline": base,
         "state_in_hbm": {"ms_per_step": round(ms_hbm, 3),
                          "GB_per_s": round(info["bytes_per_step"] / (ms_hbm * 1e-3) / 1e9, 1)},
         "state_in_host_memory": {"ms_per_step": round(ms_host, 3),
@@ -786,10 +789,15 @@ def run_state(args):
     peak, _ = measured_peaks()
     row = lambda ms, b: {"ms": round(ms, 4), "GB_per_s": round(b / (ms * 1e-3) / 1e9, 1),  # noqa
                          "frac_of_peak": round(b / (ms * 1e-3) / 1e9 / peak, 4)}
+    base = None
+    if not args.no_cpu_baseline:
+        base = {"local_step": cpu_baseline(units, info, bufs, 0, torch, seconds=2.0, n_s=1 << 20),
+                "parts": oracle_parts_baseline(W, 1 << 17)}
     print(json.dumps({"workload": "llama_block_rank0_state", "W": W, "shard_elems": S,
                       "fused_local_step": row(t_fused, b_fused), "zero1_step": row(t_zero1, b_zero1),
                       "zero1_over_fused_time": round(t_zero1 / t_fused, 3),
-                      "gather_state_f32": row(t_gather, 8 * padded), "unpack_f32": row(t_unpack, 8 * padded)}),
+                      "gather_state_f32": row(t_gather, 8 * padded), "unpack_f32": row(t_unpack, 8 * padded),
+                      "cpu_baseline": base}),
           flush=True)
 
 
@@ -827,7 +835,9 @@ def run_pipeline(args):
     link["both_ways_GB_per_s_total"] = both
     link["floor_two_way_ms"] = round((d2h_bytes / (both / 2 * 1e9) + (h2d_bytes - d2h_bytes)
                                       / (link["h2d_GB_per_s"] * 1e9)) * 1e3, 2)
+    base = None if args.no_cpu_baseline else cpu_baseline(units, info, bufs, vrank, torch, seconds=3.0)
     print(json.dumps({"workload": "llama7b_local_rank_pipeline", "W": wl.world_size, "rank": vrank,
+                      "cpu_baseline": base,
                       "host_link": link,
                       "units": info["units"], "largest_unit_params": U,
                       "h2d_bytes_per_step": 2 * wl.world_size * info["shard_elems"],
@@ -932,6 +942,52 @@ def cpu_baseline_all_ranks(units, torch, seconds=3.0, elems=1 << 20):
                       "(W=%d, F=%d: %d padded elements), every rank stepped, %d repetitions in %.1f s; "
                       "same algorithmic bytes per element" % (n_s, W, F, F * n_s, reps, dt),
             "cpu": cpu_model()}
+
+
+def oracle_rate(fn, bytes_per_call, seconds):
+    """One-core GB/s of an oracle call at its algorithmic bytes: repeated for about `seconds`."""
+    t0 = time.perf_counter()
+    reps = 0
+    while True:
+        fn()
+        reps += 1
+        if time.perf_counter() - t0 >= seconds:
+            break
+    return round(bytes_per_call * reps / (time.perf_counter() - t0) / 1e9, 4)
+
+
+def oracle_parts_baseline(W, n, seconds=1.0, seed=0):
+    """The oracle's separate calls on a seeded sample of n elements per shard (W ranks), one
+    core: reduce-scatter for one rank, Adam with the bf16 cast, the all-gather of W bf16 shards,
+    the gather of W fp32 shards (as bytes), and pack / unpack of two fp32 tensors; GB/s at each
+    call's algorithmic bytes."""
+    import numpy as np
+    import oracle
+    ora = oracle.load()
+    rng = np.random.default_rng(seed)
+    bf = lambda x: (x.astype(np.float32).view(np.uint32) >> 16).astype(np.uint16)  # noqa: E731
+    grads = [bf(rng.standard_normal(W * n) * 1e-3) for _ in range(W)]
+    p = (rng.standard_normal(n) * 0.02).astype(np.float32)
+    m = (np.abs(rng.standard_normal(n)) * 1e-4).astype(np.float32)
+    v = (np.abs(rng.standard_normal(n)) * 1e-4).astype(np.float32)
+    g = (rng.standard_normal(n) * 1e-3).astype(np.float32)
+    shards16 = [bf(rng.standard_normal(n) * 0.02) for _ in range(W)]
+    shards32 = [rng.standard_normal(n).astype(np.float32).view(np.uint16) for _ in range(W)]
+    tensors = [rng.standard_normal(W * n // 2).astype(np.float32) for _ in range(2)]
+    flat = np.concatenate(tensors)
+    out = {
+        "reduce_scatter_GB_per_s": oracle_rate(lambda: ora.reduce_scatter(grads, W, 1), (2 * W + 4) * n, seconds),
+        "adam_GB_per_s": oracle_rate(lambda: ora.adam(p, m, v, g, lr=1e-3, beta1=0.9, beta2=0.999, eps=1e-8,
+                                                      step=1), 30 * n, seconds),
+        "all_gather_GB_per_s": oracle_rate(lambda: ora.all_gather(shards16), 4 * W * n, seconds),
+        "gather_state_f32_GB_per_s": oracle_rate(lambda: ora.all_gather(shards32), 8 * W * n, seconds),
+        "pack_f32_GB_per_s": oracle_rate(lambda: ora.pack(tensors, W * n), 8 * W * n, seconds),
+        "unpack_f32_GB_per_s": oracle_rate(lambda: ora.unpack(flat, [t.shape for t in tensors]), 8 * W * n, seconds),
+    }
+    out.update({"unit": UNIT, "cores": 1, "kind": "oracle", "cpu": cpu_model(),
+                "sample": "seeded arrays of %d elements per shard, W = %d; each call repeated for %.1f s"
+                          % (n, W, seconds)})
+    return out
 
 
 def host_cores():

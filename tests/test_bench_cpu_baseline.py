@@ -158,3 +158,11 @@ def test_bench_refuses_a_gpu_count_it_was_not_launched_with():
     out = subprocess.run([sys.executable, os.path.join(root, "bench.py"), "--gpus", "2"], capture_output=True,
                          text=True, timeout=120, cwd=root)
     assert out.returncode != 0 and "nproc-per-node" in out.stderr
+
+
+def test_oracle_parts_baseline_times_every_separate_call():
+    res = bench.oracle_parts_baseline(4, 4096, seconds=0.05)
+    for key in ("reduce_scatter_GB_per_s", "adam_GB_per_s", "all_gather_GB_per_s", "gather_state_f32_GB_per_s",
+                "pack_f32_GB_per_s", "unpack_f32_GB_per_s"):
+        assert res[key] > 0, key
+    assert res["cores"] == 1 and res["kind"] == "oracle" and res["unit"] == bench.UNIT
