@@ -631,7 +631,7 @@ def run_unfused(args):
     peak, _ = measured_peaks()
     row = lambda ms, b: {"ms": round(ms, 4), "GB_per_s": round(b / (ms * 1e-3) / 1e9, 1),  # noqa
                          "frac_of_peak": round(b / (ms * 1e-3) / 1e9 / peak, 4)}
-    base = None if args.no_cpu_baseline else oracle_parts_baseline(W, 1 << 17)
+    oracle_base = None if args.no_cpu_baseline else oracle_parts_baseline(W, 1 << 17)
     print(json.dumps({
         "workload": "llama_block_all_ranks_unfused", "W": W, "padded_elems": padded,
         "reduce_scatter_x8": row(t_rs, b_rs), "adam_shard_step_x8": row(t_ad, b_ad), "all_gather": row(t_ag, b_ag),
@@ -639,7 +639,7 @@ def run_unfused(args):
         "fused": row(t_fused, (2 * W + 26) * padded),
         "fused_speedup": round((t_rs + t_ad + t_ag) / t_fused, 3),
         "pack_f32": row(t_pack, 8 * lay2.numel),
-        "bytes_per_element": {"unfused": 2 * W + 38, "fused": 2 * W + 26}, "cpu_baseline": base}), flush=True)
+        "bytes_per_element": {"unfused": 2 * W + 38, "fused": 2 * W + 26}, "cpu_baseline": oracle_base}), flush=True)
 
 
 def run_offload(args):
@@ -721,10 +721,10 @@ def run_offload(args):
     # the staged step moves 12 B per shard element each way, both directions at once
     both = host_link_both_ways(torch, h2d, d2h)
     floor_ms = 12 * S_tot / (both / 2 * 1e9) * 1e3
-    base = None if args.no_cpu_baseline else cpu_baseline(units, info, bufs, 0, torch, seconds=3.0)
+    oracle_base = None if args.no_cpu_baseline else cpu_baseline(units, info, bufs, 0, torch, seconds=3.0)
     print(json.dumps({
         "workload": "llama7b_local_rank_state_offload", "W": wl.world_size, "shard_elems": S_tot,
-        "cpu_baseline": base,
+        "cpu_baseline": oracle_base,
         "state_in_hbm": {"ms_per_step": round(ms_hbm, 3),
                          "GB_per_s": round(info["bytes_per_step"] / (ms_hbm * 1e-3) / 1e9, 1)},
         "state_in_host_memory": {"ms_per_step": round(ms_host, 3),
@@ -789,15 +789,15 @@ def run_state(args):
     peak, _ = measured_peaks()
     row = lambda ms, b: {"ms": round(ms, 4), "GB_per_s": round(b / (ms * 1e-3) / 1e9, 1),  # noqa
                          "frac_of_peak": round(b / (ms * 1e-3) / 1e9 / peak, 4)}
-    base = None
+    oracle_base = None
     if not args.no_cpu_baseline:
-        base = {"local_step": cpu_baseline(units, info, bufs, 0, torch, seconds=2.0, n_s=1 << 20),
-                "parts": oracle_parts_baseline(W, 1 << 17)}
+        oracle_base = {"local_step": cpu_baseline(units, info, bufs, 0, torch, seconds=2.0, n_s=1 << 20),
+                       "parts": oracle_parts_baseline(W, 1 << 17)}
     print(json.dumps({"workload": "llama_block_rank0_state", "W": W, "shard_elems": S,
                       "fused_local_step": row(t_fused, b_fused), "zero1_step": row(t_zero1, b_zero1),
                       "zero1_over_fused_time": round(t_zero1 / t_fused, 3),
                       "gather_state_f32": row(t_gather, 8 * padded), "unpack_f32": row(t_unpack, 8 * padded),
-                      "cpu_baseline": base}),
+                      "cpu_baseline": oracle_base}),
           flush=True)
 
 
@@ -835,9 +835,9 @@ def run_pipeline(args):
     link["both_ways_GB_per_s_total"] = both
     link["floor_two_way_ms"] = round((d2h_bytes / (both / 2 * 1e9) + (h2d_bytes - d2h_bytes)
                                       / (link["h2d_GB_per_s"] * 1e9)) * 1e3, 2)
-    base = None if args.no_cpu_baseline else cpu_baseline(units, info, bufs, vrank, torch, seconds=3.0)
+    oracle_base = None if args.no_cpu_baseline else cpu_baseline(units, info, bufs, vrank, torch, seconds=3.0)
     print(json.dumps({"workload": "llama7b_local_rank_pipeline", "W": wl.world_size, "rank": vrank,
-                      "cpu_baseline": base,
+                      "cpu_baseline": oracle_base,
                       "host_link": link,
                       "units": info["units"], "largest_unit_params": U,
                       "h2d_bytes_per_step": 2 * wl.world_size * info["shard_elems"],
