@@ -166,3 +166,20 @@ def test_oracle_parts_baseline_times_every_separate_call():
                 "pack_f32_GB_per_s", "unpack_f32_GB_per_s"):
         assert res[key] > 0, key
     assert res["cores"] == 1 and res["kind"] == "oracle" and res["unit"] == bench.UNIT
+
+
+def test_e2e_reports_unavailable_when_pinned_buffers_fail(monkeypatch):
+    """A failed page-locked allocation makes the e2e record say so (no crash, no timing)."""
+    import argparse
+
+    def fail(*a, **k):
+        raise RuntimeError("CUDA error: out of memory\nmore lines")
+
+    monkeypatch.setattr(bench, "pipeline_setup", fail)
+    args = argparse.Namespace(steps=4, e2e_steps=4, warmup=3)
+    info = dict(W=8, shard_elems=1000, bytes_per_step=70 * 1000)
+    e = bench.e2e_local_rank(args, None, None, None, None, [], info, None, 0, None, 1, None)
+    assert e["value"] is None and e["unit"] == bench.UNIT
+    assert e["h2d_bytes_per_step"] == 16 * 1000 and e["d2h_bytes_per_step"] == 2 * 1000
+    assert "could not be allocated" in e["unavailable"] and "out of memory" in e["unavailable"]
+    assert "more lines" not in e["unavailable"]
