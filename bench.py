@@ -1052,12 +1052,10 @@ def run_reference(args):
     import oracle
     import synth
     from synth import workloads as wls
-    import fully_sharded_gb300 as fs
-    ora = oracle.load()
+    ora = oracle.load()  # the oracle alone: the CUDA library is not loaded on this arm
     wl = wls.LLAMA7B
     W = wl.world_size
-    lay = fs.fsdp_flatten_layout(wls.numels(wl.units[0]), W)[0]
-    S = lay.shard_numel
+    _, _, _, S = ora.flatten_layout(wls.numels(wl.units[0]), W)
     n_s = args.ref_sample
     r = 0
     grads = np.zeros((W, W * n_s), dtype=np.uint16)

@@ -34,7 +34,7 @@ FSDP_EINVAL = -1
 FSDP_EALIAS = -2
 FSDP_ECUDA = -3
 FSDP_ENOSPACE = -4
-NOALLOC_STAGING_BYTES = 64 << 20
+NOALLOC_STAGING_BYTES = 64 << 20  # FSDP_NOALLOC_STAGING_BYTES of include/fsdp.h
 FSDP_DTYPE_F32 = 0
 FSDP_DTYPE_BF16 = 1
 MAX_WORLD = 64
@@ -383,9 +383,10 @@ def fsdp_offload_step(units, rank: int, staging, slot_numel: int, n_slots: int, 
 def fsdp_pipeline_step_noalloc(units, rank: int, n_slots: int, adam: AdamHyper, compute=None,
                                copy=None):
     """fsdp_pipeline_step without a staging argument, for callers that cannot allocate
-    device memory when they step: the pool is a fixed 64 MiB array inside the library
-    (FsdpError with status FSDP_ENOSPACE if n_slots times the largest unit does not fit).
-    Calls on one device share that array, so their GPU work must not overlap."""
+    device memory when they step: the pool is a fixed array of NOALLOC_STAGING_BYTES
+    inside the library (FsdpError with status FSDP_ENOSPACE if n_slots times the largest
+    unit, rounded up to 8 elements, does not fit). Calls on one device share that array,
+    so their GPU work must not overlap."""
     batch = units if isinstance(units, PipelineBatch) else PipelineBatch(units)
     _check("fsdp_pipeline_step_noalloc", _lib.fsdp_pipeline_step_noalloc(
         batch.array, batch.n, rank, n_slots, ctypes.byref(adam), _stream(compute), _stream(copy)))
@@ -432,7 +433,8 @@ def fsdp_device_status(clear: bool = False) -> int:
 
 
 def fsdp_selftest_wait_timeout(src, dst, wait_limit_ns: int, stream=None) -> int:
-    """Provokes one bounded-wait timeout on a copy of src into dst; returns the status word seen."""
+    """Diagnostic call of include/fsdp_test.h (not part of the method's interface):
+    provokes one bounded-wait timeout on a copy of src into dst; returns the status word seen."""
     v = ctypes.c_uint32(0)
     nbytes = src.numel() * src.element_size()
     _check("fsdp_selftest_wait_timeout", _lib.fsdp_selftest_wait_timeout(

@@ -1,9 +1,11 @@
-// GPU entry points of the C ABI (include/fsdp.h): argument validation, alias
+// GPU entry points of the C ABI (include/fsdp.h, and the diagnostic call of
+// include/fsdp_test.h): argument validation, alias
 // checks, segment-table construction and launch of the segment kernel.
 //
 // Nothing here allocates device memory: each launch carries its descriptor
 // table as a __grid_constant__ kernel parameter.
 #include "fsdp.h"
+#include "fsdp_test.h"
 #include "segment_kernel.cuh"
 #include "host_internal.h"
 

@@ -10,6 +10,7 @@
 
 #include <cstdint>
 #include <limits>
+#include <string>
 
 extern "C" int fsdp_flatten_layout(const int64_t* numels, int32_t n_tensors, int32_t world_size,
                                    int32_t shard_factor, int64_t* offsets_out,
@@ -80,13 +81,26 @@ extern "C" int fsdp_account_zero(double P, int32_t N, int32_t stage, fsdp_zero_a
   return FSDP_OK;
 }
 
+namespace {
+
+// The capacity in the message is FSDP_NOALLOC_STAGING_BYTES itself, so the two
+// cannot disagree (built once, thread-safe static initialisation).
+const char* enospace_text() {
+  static const std::string text =
+      "work exceeds the " + std::to_string(FSDP_NOALLOC_STAGING_BYTES >> 20) +
+      " MiB staging capacity of the allocation-free entry point";
+  return text.c_str();
+}
+
+}  // namespace
+
 extern "C" const char* fsdp_status_string(int status) {
   switch (status) {
     case FSDP_OK: return "ok";
     case FSDP_EINVAL: return "invalid argument";
     case FSDP_EALIAS: return "an output overlaps an input or another output";
     case FSDP_ECUDA: return "CUDA launch error";
-    case FSDP_ENOSPACE: return "work exceeds the 64 MiB staging capacity of the allocation-free entry point";
+    case FSDP_ENOSPACE: return enospace_text();
     default: return "unknown status";
   }
 }

@@ -56,6 +56,10 @@ extern "C" int fsdp_pipeline_step_noalloc(const fsdp_pipeline_unit_t* units, int
     if (!units[i].layout || units[i].layout->padded_numel < 0) return FSDP_EINVAL;
     if (units[i].layout->padded_numel > slot) slot = units[i].layout->padded_numel;
   }
+  // every slot starts 16-byte aligned (whole 8-element groups), so a unit whose
+  // own rows are aligned keeps the vector path in any slot
+  if (slot > fsdp::kStagingElems) return FSDP_ENOSPACE;
+  slot = (slot + 7) / 8 * 8;
   if (slot > fsdp::kStagingElems / n_slots) return FSDP_ENOSPACE;
   uint16_t* staging = nullptr;
   if (int rc = fsdp::staging_address(&staging)) return rc;

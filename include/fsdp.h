@@ -26,13 +26,18 @@
  *   [gloss] glossary entry "fully sharded data parallel fsdp"
  *
  * Conventions for every call:
- *   - The caller owns all memory. The library allocates nothing and keeps no
- *     state about the data between calls (it caches the SM count and kernel
- *     occupancy per device; fsdp_pipeline_step and fsdp_offload_step create
- *     and release CUDA events within a call; fsdp_pipeline_step_noalloc stages
- *     through a fixed array that is part of the library's device code, see
- *     there; a per-device status word records a device wait that ran out, see
- *     fsdp_device_status).
+ *   - The caller owns all memory of the data. No call allocates, and the
+ *     library keeps no state about the data between calls (it caches the SM
+ *     count and kernel occupancy per device; fsdp_pipeline_step and
+ *     fsdp_offload_step create and release CUDA events within a call; a
+ *     per-device status word records a device wait that ran out, see
+ *     fsdp_device_status). One fixed device array is part of the library's
+ *     device code: the staging pool of fsdp_pipeline_step_noalloc, of
+ *     FSDP_NOALLOC_STAGING_BYTES. The CUDA runtime reserves it on every GPU
+ *     where it loads the library's device code, whether or not that entry
+ *     point is ever called, and keeps it until the process exits.
+ *   - Diagnostic calls that drive failure paths on purpose are declared in
+ *     fsdp_test.h, not here.
  *   - "device" pointers point to CUDA global memory of the current device;
  *     pointer arrays themselves (const T* const*) are HOST arrays of device
  *     pointers and are read before the call returns.
@@ -121,14 +126,24 @@ int fsdp_flatten_layout(const int64_t *numels, int32_t n_tensors, int32_t world_
                         int32_t shard_factor, int64_t *offsets_out, fsdp_layout_t *out);
 
 /* a2. Pack tensors into the flat buffer (one launch), zero-filling the pad.
+ * [math] "The sharding unit: FlatParameter and the wrapping policy": a unit's
+ * parameters are flattened into one contiguous 1-D buffer (row-major, in the
+ * listed order) that splits evenly over the ranks.
  * tensors: host array of n_tensors device pointers (contiguous tensors of the
  * element type `dtype`); offsets: the host array fsdp_flatten_layout wrote;
  * flat_out: device buffer of padded_numel elements. Pad elements become +0.0
- * (all-zero bits). EALIAS if flat_out overlaps a tensor. */
+ * (all-zero bits). EINVAL: a bad layout, dtype or offsets, a null pointer;
+ * EALIAS if flat_out overlaps a tensor. */
 int fsdp_pack_flat(const void *const *tensors, const fsdp_layout_t *layout,
                    const int64_t *offsets, int32_t dtype, void *flat_out, fsdp_stream_t stream);
 
-/* a2. Unpack: copy each tensor's range of the flat buffer back out (pad dropped). */
+/* a2. Unpack: copy each tensor's range of the flat buffer back out (pad dropped).
+ * [math] "The sharding unit: FlatParameter and the wrapping policy": the
+ * tensors are views of their ranges of the FlatParameter; this is the inverse
+ * of fsdp_pack_flat. flat: device buffer of padded_numel elements of `dtype`;
+ * tensors_out: host array of n_tensors device pointers, tensor i receives
+ * elements [offsets[i], offsets[i+1]). EINVAL as for fsdp_pack_flat; EALIAS if
+ * a tensor overlaps the flat buffer or another tensor. */
 int fsdp_unpack_flat(const void *flat, const fsdp_layout_t *layout, const int64_t *offsets,
                      int32_t dtype, void *const *tensors_out, fsdp_stream_t stream);
 
@@ -240,16 +255,6 @@ int fsdp_shard_step_grouped_plan(const fsdp_unit_args_t *units, int32_t n_units,
  * valid. This does not happen in a correct run. clear != 0 resets the word
  * after reading it. EINVAL: status_out NULL; ECUDA: the read failed. */
 int fsdp_device_status(int32_t clear, uint32_t *status_out);
-
-/* Self-test of the bounded waits: launches the TMA form on a copy of `bytes`
- * (>= 16384, <= 2^30, both pointers 16-byte aligned, not overlapping) with
- * block 0's first stage expecting 16 bytes that no copy delivers, and a wait
- * limit of wait_limit_ns (1 ns .. 10 s). The block gives up after the limit,
- * drains its copies and returns; the call synchronizes `stream`, then reads
- * and clears the status word into *status_out (1 when the timeout was seen).
- * dst is partly written. Nothing hangs and the context stays usable. */
-int fsdp_selftest_wait_timeout(const void *src, void *dst, int64_t bytes, int64_t wait_limit_ns,
-                               fsdp_stream_t stream, uint32_t *status_out);
 
 /* Pipelined step of one rank over many units (full sharding, F = W), with a
  * bounded pool of staging slots for the incoming gradients.
@@ -365,7 +370,8 @@ int fsdp_offload_step(const fsdp_offload_unit_t *units, int32_t n_units, int32_t
  * runtime reserves on a GPU when it loads that code there and keeps until the
  * process exits. The call itself allocates nothing.
  * Same arguments and results as fsdp_pipeline_step, with slot_numel = the
- * largest padded_numel among the units. FSDP_ENOSPACE (nothing launched) if
+ * largest padded_numel among the units rounded up to a multiple of 8 (so every
+ * slot starts 16-byte aligned). FSDP_ENOSPACE (nothing launched) if
  * n_slots * slot_numel * 2 exceeds FSDP_NOALLOC_STAGING_BYTES.
  * The first call on a device looks up the array's device address (with that
  * device current); make that first call before any stream capture. Every

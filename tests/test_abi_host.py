@@ -102,8 +102,28 @@ def test_account_rejects():
 
 def test_status_strings():
     assert fs.fsdp_status_string(0) == "ok"
-    for s in (fs.FSDP_EINVAL, fs.FSDP_EALIAS, fs.FSDP_ECUDA):
+    for s in (fs.FSDP_EINVAL, fs.FSDP_EALIAS, fs.FSDP_ECUDA, fs.FSDP_ENOSPACE):
         assert fs.fsdp_status_string(s) not in ("ok", "unknown status")
+
+
+def test_noalloc_capacity_agrees_across_header_binding_and_message():
+    """The allocation-free entry point's capacity has one definition (the header's macro):
+    the binding's constant and the FSDP_ENOSPACE text both follow it."""
+    text = open(os.path.join(ROOT, "include", "fsdp.h")).read()
+    m = re.search(r"#define\s+FSDP_NOALLOC_STAGING_BYTES\s+\((\d+)ll\s*<<\s*(\d+)\)", text)
+    assert m, "FSDP_NOALLOC_STAGING_BYTES not found in the header"
+    assert int(m.group(1)) << int(m.group(2)) == fs.NOALLOC_STAGING_BYTES
+    assert "%d MiB" % (fs.NOALLOC_STAGING_BYTES >> 20) in fs.fsdp_status_string(fs.FSDP_ENOSPACE)
+
+
+def test_diagnostic_call_is_declared_apart_from_the_method():
+    """The bounded-wait self-test is exported but declared in the diagnostic header only."""
+    def decls(name):
+        t = re.sub(r"/\*.*?\*/", "", open(os.path.join(ROOT, "include", name)).read(), flags=re.S)
+        return set(re.findall(r"\b(fsdp_\w+)\s*\(", t))
+    assert "fsdp_selftest_wait_timeout" in decls("fsdp_test.h")
+    assert "fsdp_selftest_wait_timeout" not in decls("fsdp.h")
+    assert hasattr(ctypes.CDLL(fs.library_path()), "fsdp_selftest_wait_timeout")
 
 
 # ---------------------------------------------- GPU entry points, rejected

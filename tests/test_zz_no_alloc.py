@@ -7,8 +7,13 @@ results as fsdp_pipeline_step with a caller-owned staging pool, call after
 call, since every call reuses the library's fixed staging array. This file is
 collected last so that a run stopping at its first failure has run every
 other test before it; it also passes when run on its own.
+
+The cases vary the world size and the number of slots: W = 8 with two slots;
+W = 2 with one slot and a first unit of more than 4 M shard elements, which
+moves through the shared array in pieces; W = 4 with three slots, where the
+largest unit's padded length is not a multiple of 8 elements and a smaller,
+aligned unit lands in slot 1.
 """
-import numpy as np
 import pytest
 
 import gpu_util as gu
@@ -18,8 +23,12 @@ pytestmark = pytest.mark.gpu
 
 fs = pytest.importorskip("fully_sharded_gb300")
 
-W, RANK, N_SLOTS = 8, 5, 2
-SIZES = [7087872, 8 * 100003, 8 * 4096 + 3]  # a GPT-2-small block, a ragged unit, a small one
+CASES = {
+    # name: (W, rank, n_slots, unit sizes P)
+    "w8_two_slots": (8, 5, 2, [7087872, 8 * 100003, 8 * 4096 + 3]),
+    "w2_one_slot_pieces": (2, 1, 1, [2 * 5_000_001, 2 * 65536]),
+    "w4_three_slots_ragged": (4, 2, 3, [4 * 1_000_001, 4 * 65536, 4 * 3001 + 1]),
+}
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -29,33 +38,38 @@ def _cuda():
         pytest.skip("needs a CUDA GPU")
 
 
-def _units(base):
+def _units(W, rank, sizes, base):
     torch = gu.torch()
     units = []
-    for u, P in enumerate(SIZES):
+    for u, P in enumerate(sizes):
         lay, _ = fs.fsdp_flatten_layout([P], W)
         S, padded = lay.shard_numel, lay.padded_numel
         key = lambda *f: synth.stream_key(base, u, *f)  # noqa: E731
         units.append(dict(
             layout=lay,
-            master=gu.dev_normal(key(1), S, 0.02, idx0=RANK * S, n_valid=P),
-            exp_avg=gu.dev_normal(key(2), S, 1e-4, idx0=RANK * S, absval=True, n_valid=P),
-            exp_avg_sq=gu.dev_normal(key(3), S, 1e-4, idx0=RANK * S, absval=True, n_valid=P),
-            other_shards=[None if k == RANK else gu.dev_normal(key(5), S, 0.02, idx0=k * S, n_valid=P, bf16=True)
+            master=gu.dev_normal(key(1), S, 0.02, idx0=rank * S, n_valid=P),
+            exp_avg=gu.dev_normal(key(2), S, 1e-4, idx0=rank * S, absval=True, n_valid=P),
+            exp_avg_sq=gu.dev_normal(key(3), S, 1e-4, idx0=rank * S, absval=True, n_valid=P),
+            other_shards=[None if k == rank else gu.dev_normal(key(5), S, 0.02, idx0=k * S, n_valid=P, bf16=True)
                           for k in range(W)],
             full_out=torch.zeros(padded, dtype=torch.int16, device="cuda"),
             shard_out=torch.zeros(S, dtype=torch.int16).pin_memory()))
     return units
 
 
-def _set_grads(units, base, step):
+def _set_grads(units, W, rank, base, step):
+    """The step's gradient slices, drawn by the device generator into pinned host memory."""
     torch = gu.torch()
     for u, unit in enumerate(units):
         lay = unit["layout"]
         S, P = lay.shard_numel, lay.numel
-        rows = [synth.normal_bf16(synth.stream_key(base, u, 4, k, step), S, 1e-2, idx0=RANK * S, n_valid=P)
-                for k in range(W)]
-        unit["grad_slices"] = torch.from_numpy(np.stack(rows).view(np.int16)).pin_memory()
+        rows = torch.empty((W, S), dtype=torch.int16, device="cuda")
+        for k in range(W):
+            synth.fill_(rows[k], synth.stream_key(base, u, 4, k, step), 1e-2, idx0=rank * S, n_valid=P)
+        host = torch.empty((W, S), dtype=torch.int16).pin_memory()
+        host.copy_(rows)
+        unit["grad_slices"] = host
+    torch.cuda.synchronize()
 
 
 def _copy_units(units):
@@ -69,34 +83,41 @@ def _copy_units(units):
     return out
 
 
-def test_noalloc_matches_pipeline_on_two_calls():
+@pytest.mark.parametrize("case", list(CASES))
+def test_noalloc_matches_pipeline_on_two_calls(case):
     torch = gu.torch()
-    base = 9100
-    ref = _units(base)
+    W, rank, n_slots, sizes = CASES[case]
+    base = 9100 + 10 * list(CASES).index(case)
+    ref = _units(W, rank, sizes, base)
     got = _copy_units(ref)
     slot = max(u["layout"].padded_numel for u in ref)
-    staging = torch.empty(N_SLOTS * slot, dtype=torch.int16, device="cuda")
+    slot = (slot + 7) // 8 * 8  # the caller-owned pool gets the same aligned slots
+    assert n_slots * slot * 2 <= fs.NOALLOC_STAGING_BYTES
+    staging = torch.empty(n_slots * slot, dtype=torch.int16, device="cuda")
     compute, copy = torch.cuda.Stream(), torch.cuda.Stream()
     for step in (1, 2):
-        _set_grads(ref, base, step)
+        _set_grads(ref, W, rank, base, step)
         for g, r in zip(got, ref):
             g["grad_slices"] = r["grad_slices"]
         hp = gu.adam_hyper(step)
-        fs.fsdp_pipeline_step(ref, RANK, staging, slot, N_SLOTS, hp, compute=compute, copy=copy)
-        fs.fsdp_pipeline_step_noalloc(got, RANK, N_SLOTS, hp, compute=compute, copy=copy)
+        fs.fsdp_pipeline_step(ref, rank, staging, slot, n_slots, hp, compute=compute, copy=copy)
+        fs.fsdp_pipeline_step_noalloc(got, rank, n_slots, hp, compute=compute, copy=copy)
         torch.cuda.synchronize()
-        for g, r in zip(got, ref):
+        for u, (g, r) in enumerate(zip(got, ref)):
             for name in ("master", "exp_avg", "exp_avg_sq"):
                 a, b = gu.to_host(g[name]), gu.to_host(r[name])
-                gu.assert_f32_close(a, b, "%s step %d" % (name, step))
-                gu.assert_same_bits(a, b, "%s step %d" % (name, step))
-            gu.assert_bf16_close(gu.to_host(g["full_out"]), gu.to_host(r["full_out"]), "full step %d" % step)
-            gu.assert_same_bits(g["shard_out"].numpy(), r["shard_out"].numpy(), "shard_out step %d" % step)
+                gu.assert_f32_close(a, b, "%s unit %d step %d" % (name, u, step))
+                gu.assert_same_bits(a, b, "%s unit %d step %d" % (name, u, step))
+            gu.assert_bf16_close(gu.to_host(g["full_out"]), gu.to_host(r["full_out"]),
+                                 "full unit %d step %d" % (u, step))
+            gu.assert_same_bits(g["shard_out"].numpy(), r["shard_out"].numpy(),
+                                "shard_out unit %d step %d" % (u, step))
 
 
 def test_noalloc_rejects_work_beyond_its_capacity():
     torch = gu.torch()
-    P = fs.NOALLOC_STAGING_BYTES // 2 // N_SLOTS + 8  # one slot's worth too large for two slots
+    W, rank, n_slots = 8, 5, 2
+    P = fs.NOALLOC_STAGING_BYTES // 2 // n_slots + 8  # one slot's worth too large for two slots
     lay, _ = fs.fsdp_flatten_layout([P], W)
     S = lay.shard_numel
     small = torch.zeros(8, device="cuda")
@@ -105,6 +126,6 @@ def test_noalloc_rejects_work_beyond_its_capacity():
                 shard_out=None)
     assert S > 0
     with pytest.raises(fs.FsdpError) as e:
-        fs.fsdp_pipeline_step_noalloc([unit], RANK, N_SLOTS, gu.adam_hyper(1))
+        fs.fsdp_pipeline_step_noalloc([unit], rank, n_slots, gu.adam_hyper(1))
     assert e.value.status == fs.FSDP_ENOSPACE
-    assert "64 MiB" in fs.fsdp_status_string(fs.FSDP_ENOSPACE)
+    assert "%d MiB" % (fs.NOALLOC_STAGING_BYTES >> 20) in fs.fsdp_status_string(fs.FSDP_ENOSPACE)
