@@ -134,7 +134,8 @@ def _load():
         "fsdp_zero1_step": [P, ctypes.POINTER(Layout), _c_i32, P, P, P, P, P, P, ctypes.POINTER(AdamHyper), P],
         "fsdp_account_zero": [_c_dbl, _c_i32, _c_i32, ctypes.POINTER(ZeroAccount)],
         "fsdp_shard_step_grouped_plan": [ctypes.POINTER(UnitArgs), _c_i32, _c_i32, _c_i32,
-                                         ctypes.POINTER(_c_i32), ctypes.POINTER(_c_i32)],
+                                         ctypes.POINTER(_c_i32), ctypes.POINTER(_c_i32),
+                                         ctypes.POINTER(_c_i32)],
         "fsdp_device_status": [_c_i32, ctypes.POINTER(ctypes.c_uint32)],
         "fsdp_selftest_wait_timeout": [P, P, _c_i64, _c_i64, P, ctypes.POINTER(ctypes.c_uint32)],
         "fsdp_offload_step": [ctypes.POINTER(OffloadUnit), _c_i32, _c_i32, P, _c_i64, _c_i32,
@@ -416,13 +417,15 @@ def fsdp_account_zero(P: float, N: int, stage: int) -> dict:
     return out.as_dict()
 
 
-def fsdp_shard_step_grouped_plan(units, rank_begin: int, rank_end: int):
-    """Host only: (launches, launches in the TMA form) of fsdp_shard_step_grouped for these units."""
+def fsdp_shard_step_grouped_plan(units, rank_begin: int, rank_end: int, interleaved: bool = False):
+    """Host only: (launches, launches in the TMA form) of fsdp_shard_step_grouped for these
+    units; with interleaved=True also the number of TMA launches that stage their step
+    chunks in interleaved quarter-chunk copies."""
     batch = units if isinstance(units, UnitBatch) else UnitBatch(units)
-    n, t = _c_i32(0), _c_i32(0)
+    n, t, i = _c_i32(0), _c_i32(0), _c_i32(0)
     _check("fsdp_shard_step_grouped_plan", _lib.fsdp_shard_step_grouped_plan(
-        batch.array, batch.n, rank_begin, rank_end, ctypes.byref(n), ctypes.byref(t)))
-    return n.value, t.value
+        batch.array, batch.n, rank_begin, rank_end, ctypes.byref(n), ctypes.byref(t), ctypes.byref(i)))
+    return (n.value, t.value, i.value) if interleaved else (n.value, t.value)
 
 
 def fsdp_device_status(clear: bool = False) -> int:

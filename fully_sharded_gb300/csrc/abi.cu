@@ -202,9 +202,11 @@ bool wants_interleave(const Params& p) {
 
 }  // namespace
 
-int launch(const SegmentList& list, const Scalars& s, cudaStream_t stream, int* count, int* tma_count) {
+int launch(const SegmentList& list, const Scalars& s, cudaStream_t stream, int* count, int* tma_count,
+           int* interleaved_count) {
   if (count) *count = 0;
   if (tma_count) *tma_count = 0;
+  if (interleaved_count) *interleaved_count = 0;
   if (list.seg.empty()) return FSDP_OK;
   const int variant = variant_of(s.w);
   int err = FSDP_OK;
@@ -249,6 +251,7 @@ int launch(const SegmentList& list, const Scalars& s, cudaStream_t stream, int* 
     if (count) {
       ++*count;
       if (tma && tma_count) ++*tma_count;
+      if (tma && interleaved_count && wants_interleave(p)) ++*interleaved_count;
       continue;
     }
     if (tma) {
@@ -378,9 +381,11 @@ using namespace fsdp;
 namespace {
 
 int grouped(const fsdp_unit_args_t* units, int32_t n_units, int32_t rank_begin, int32_t rank_end,
-            const fsdp_adam_t* adam, cudaStream_t stream, int* count, int* tma_count = nullptr) {
+            const fsdp_adam_t* adam, cudaStream_t stream, int* count, int* tma_count = nullptr,
+            int* interleaved_count = nullptr) {
   if (count) *count = 0;
   if (tma_count) *tma_count = 0;
+  if (interleaved_count) *interleaved_count = 0;
   if (n_units < 0 || (n_units > 0 && !units)) return FSDP_EINVAL;
   if (n_units == 0) return FSDP_OK;
   const fsdp_layout_t* L0 = units[0].layout;
@@ -402,7 +407,7 @@ int grouped(const fsdp_unit_args_t* units, int32_t n_units, int32_t rank_begin, 
     if (int rc = build_unit(units[i], rank_begin, rank_end, list, alias)) return rc;
   }
   if (!alias.ok()) return FSDP_EALIAS;
-  return launch(list, s, stream, count, tma_count);
+  return launch(list, s, stream, count, tma_count, interleaved_count);
 }
 
 }  // namespace
@@ -417,17 +422,19 @@ extern "C" int fsdp_shard_step_grouped(const fsdp_unit_args_t* units, int32_t n_
 extern "C" int fsdp_shard_step_grouped_launches(const fsdp_unit_args_t* units, int32_t n_units,
                                                 int32_t rank_begin, int32_t rank_end,
                                                 int32_t* launches_out) {
-  return fsdp_shard_step_grouped_plan(units, n_units, rank_begin, rank_end, launches_out, nullptr);
+  return fsdp_shard_step_grouped_plan(units, n_units, rank_begin, rank_end, launches_out, nullptr, nullptr);
 }
 
 extern "C" int fsdp_shard_step_grouped_plan(const fsdp_unit_args_t* units, int32_t n_units, int32_t rank_begin,
-                                            int32_t rank_end, int32_t* launches_out, int32_t* tma_launches_out) {
+                                            int32_t rank_end, int32_t* launches_out, int32_t* tma_launches_out,
+                                            int32_t* tma_interleaved_out) {
   if (!launches_out) return FSDP_EINVAL;
-  int count = 0, tma = 0;
-  const int rc = grouped(units, n_units, rank_begin, rank_end, nullptr, nullptr, &count, &tma);
+  int count = 0, tma = 0, interleaved = 0;
+  const int rc = grouped(units, n_units, rank_begin, rank_end, nullptr, nullptr, &count, &tma, &interleaved);
   if (rc == FSDP_OK) {
     *launches_out = count;
     if (tma_launches_out) *tma_launches_out = tma;
+    if (tma_interleaved_out) *tma_interleaved_out = interleaved;
   }
   return rc;
 }

@@ -119,9 +119,11 @@ struct EventSet {
 
 // Launch the list, splitting it where a descriptor table would overflow. With
 // `count` set, nothing is launched and the number of launches is returned there.
-// `tma_count`, if set, receives how many of those launches use the TMA form.
+// `tma_count`, if set, receives how many of those launches use the TMA form,
+// and `interleaved_count` how many of those stage their step chunks in
+// interleaved quarter-chunk copies (the second instantiation of the TMA form).
 int launch(const SegmentList& list, const Scalars& s, cudaStream_t stream, int* count = nullptr,
-           int* tma_count = nullptr);
+           int* tma_count = nullptr, int* interleaved_count = nullptr);
 
 // Layout consistent with its own definition (padding, shard length, W, F).
 bool layout_ok(const fsdp_layout_t* L);

@@ -242,11 +242,14 @@ int fsdp_shard_step_grouped_launches(const fsdp_unit_args_t *units, int32_t n_un
  * receives how many of those launches use the TMA form of the kernel (bulk
  * copies into a shared-memory pipeline; chosen for W = 8 launches made of
  * one-replica step segments, and copies, with enough chunks to fill every SM's
- * pipeline). Needs no GPU, but reads the SM count of the current device when
- * one is present. */
+ * pipeline), *tma_interleaved_out (if not NULL) how many of the TMA launches
+ * stage their step chunks in four interleaved rounds of quarter-chunk copies
+ * (chosen when a launch's gradient rows span 3 GiB or more of addresses).
+ * Needs no GPU, but reads the SM count of the current device when one is
+ * present. */
 int fsdp_shard_step_grouped_plan(const fsdp_unit_args_t *units, int32_t n_units,
                                  int32_t rank_begin, int32_t rank_end, int32_t *launches_out,
-                                 int32_t *tma_launches_out);
+                                 int32_t *tma_launches_out, int32_t *tma_interleaved_out);
 
 /* The current device's sticky status word, read after all work of the
  * device, on every stream, has finished (the call synchronizes the device). Bit 0 is

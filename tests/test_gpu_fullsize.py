@@ -1,15 +1,20 @@
-"""Full-size workloads, in the launch configuration the benchmark times, checked on samples.
+"""Full-size workloads, in the launch configuration the benchmark times.
 
-Inputs are filled on the device by the seeded generator; the host regenerates
-the inputs at sampled positions (first/last elements of every shard, chunk and
-tensor boundaries, random positions), the oracle computes those outputs one by
-one, and they must equal the device outputs bit for bit. The hybrid workload
-is also checked for bit-identical parameters across F = 1, 4, 16 on every
-element.
+Inputs are filled on the device by the seeded generator. The headline launch
+(the Llama-7B local-rank step, which runs the TMA form with interleaved copies)
+and the 1e9-element W = 8 step on the same instantiation are compared with the
+oracle on every element of the checked units (tests/full_parity.py runs the
+oracle on all host cores). The other workloads are checked on samples: the
+host regenerates the inputs at sampled positions (first/last elements of every
+shard, chunk and tensor boundaries, random positions), the oracle computes
+those outputs one by one, and they must equal the device outputs bit for bit.
+The hybrid workload is also checked for bit-identical parameters across
+F = 1, 4, 16 on every element.
 """
 import numpy as np
 import pytest
 
+import full_parity
 import gpu_util as gu
 import synth
 from synth import workloads as wls
@@ -105,18 +110,39 @@ def test_gpt2_small_grouped(ora):
     del units, keep
 
 
-@pytest.mark.parametrize("W", [2, 4, 8, 16])
+def test_sweep_1e9_w8_every_element(ora):
+    """One FlatParameter of 1e9 elements stepped for all 8 ranks in one launch of the TMA form
+    with interleaved copies (the gradient rows are 2 GB apart), as the size sweep times it:
+    every element of every rank's master, exp_avg, exp_avg_sq and of the full bf16 buffer
+    equals the oracle's shard_step."""
+    torch = gu.torch()
+    n, W = 1_000_000_000, 8
+    wl = bench.sweep_workload(n, W)
+    units, info, keep = bench.build_all_ranks(wl, W, torch, fs, synth)
+    assert fs.fsdp_shard_step_grouped_plan(units, 0, W, interleaved=True) == (1, 1, 1)
+    fs.fsdp_shard_step_grouped(units, 0, W, gu.adam_hyper(2))
+    torch.cuda.synchronize()
+    assert fs.fsdp_device_status() == 0
+    lay = units[0]["layout"]
+    S = lay.shard_numel
+    regen = full_parity.state_regen(wl, 0, lay.numel)(S)
+    done = full_parity.check_unit_every_element(ora, units[0], 0, W, 2, regen, "sweep 1e9 W=8", piece=1 << 19)
+    assert done == S
+    del units, keep
+    torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("W", [2, 4, 16])
 def test_sweep_1e9_all_ranks(ora, W):
-    """One FlatParameter of 1e9 elements stepped for all W ranks, as the size sweep times it:
-    the LDG form at W = 2, 4, 16 and the TMA form with interleaved copies at W = 8 (rows 2 GB
-    apart). Sampled outputs of every rank, plus positions around each 2 GiB boundary of the
-    flat fp32 state, equal the oracle's."""
+    """One FlatParameter of 1e9 elements stepped for all W ranks on the LDG form, as the size
+    sweep times it. Sampled outputs of every rank, plus positions around each 2 GiB boundary
+    of the flat fp32 state, equal the oracle's (W = 8 is compared on every element above)."""
     torch = gu.torch()
     n = 1_000_000_000
     wl = bench.sweep_workload(n, W)
     units, info, keep = bench.build_all_ranks(wl, W, torch, fs, synth)
     launches, tma = fs.fsdp_shard_step_grouped_plan(units, 0, W)
-    assert launches == 1 and tma == (1 if W == 8 else 0)
+    assert launches == 1 and tma == 0
     fs.fsdp_shard_step_grouped(units, 0, W, gu.adam_hyper(2))
     torch.cuda.synchronize()
     padded = units[0]["layout"].padded_numel
@@ -177,36 +203,26 @@ def test_flat_parameter_beyond_2_to_the_31_elements(ora, W, F, S):
     torch.cuda.empty_cache()
 
 
-def test_llama7b_local_rank(ora):
-    """The benchmark's headline workload and launch: one grouped launch over 33 units, rank 0."""
+def test_llama7b_local_rank_every_element(ora):
+    """The benchmark's headline workload and launch: one grouped launch over 33 units, rank 0,
+    on the TMA form with interleaved copies. For units 0, 1, 16, 31 and the root unit 32,
+    every element of the rank's master, exp_avg, exp_avg_sq, its own bf16 slice and the seven
+    gathered slices equals the oracle's shard_step."""
     torch = gu.torch()
     wl = wls.LLAMA7B
     rank = 0
     units, info, bufs = bench.build_local_rank(wl, rank, torch, fs, synth)
     assert info["params"] == 6738415616 and info["shard_elems"] == 842301952
-    assert fs.fsdp_shard_step_grouped_launches(units, rank, rank + 1) == 1
+    assert fs.fsdp_shard_step_grouped_plan(units, rank, rank + 1, interleaved=True) == (1, 1, 1)
     fs.fsdp_shard_step_grouped(units, rank, rank + 1, gu.adam_hyper(1))
     torch.cuda.synchronize()
-    W = wl.world_size
-    for u in (0, 1, 17, 31, 32):
-        unit = units[u]
-        lay = unit["layout"]
-        S, P = lay.shard_numel, lay.numel
-        j = sample_positions(S, seed=100 + u)
-        i = rank * S + j
-        rows = [synth.normal_bf16_at(wls.key_grad(wl, u % 2, k, 0), i, wl.sigma_grad) for k in range(W)]
-        master = synth.normal_f32_at(wls.key_master(wl, u), i, wl.sigma_master, n_valid=P)
-        m = synth.normal_f32_at(wls.key_exp_avg(wl, u), i, wl.sigma_state, absval=True, n_valid=P)
-        v = synth.normal_f32_at(wls.key_exp_avg_sq(wl, u), i, wl.sigma_state, absval=True, n_valid=P)
-        op, om, ov, obf = oracle_at(ora, rows, master, m, v, 1)
-        gu.assert_same_bits(gather(unit["master"][0], j), op, "master u%d" % u)
-        gu.assert_same_bits(gather(unit["exp_avg"][0], j), om, "exp_avg u%d" % u)
-        gu.assert_same_bits(gather(unit["exp_avg_sq"][0], j), ov, "exp_avg_sq u%d" % u)
-        gu.assert_same_bits(gather(unit["full_out"][0], i), obf, "own slice u%d" % u)
-        # gathered slices of the other ranks: copies of their shards
-        for k in (1, W - 1):
-            jk = sample_positions(S, k=64, seed=200 + u + k)
-            want = synth.normal_bf16_at(wls.key_shard(wl, u), k * S + jk, wl.sigma_master, n_valid=P)
-            gu.assert_same_bits(gather(unit["full_out"][0], k * S + jk), want, "gathered u%d k%d" % (u, k))
+    assert fs.fsdp_device_status() == 0
+    for u in (0, 1, 16, 31, 32):
+        lay = units[u]["layout"]
+        S = lay.shard_numel
+        regen = full_parity.state_regen(wl, u, lay.numel)(S)
+        done = full_parity.check_unit_every_element(ora, units[u], rank, rank + 1, 1, regen,
+                                                    "llama7b unit %d" % u)
+        assert done == S
     del units, bufs
     torch.cuda.empty_cache()

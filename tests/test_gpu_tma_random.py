@@ -10,11 +10,13 @@ the device by the seeded generator; the host regenerates them at sampled
 positions (the ends of every shard, chunk boundaries, random positions), the
 oracle computes those outputs, and they must equal the device's bit for bit.
 Two more local-rank cases space the gradient rows widely enough for the
-library to pick the interleaved-copy staging.
+library to pick the interleaved-copy staging; those are compared on every
+element.
 """
 import numpy as np
 import pytest
 
+import full_parity
 import gpu_util as gu
 import synth
 from synth import workloads as wls
@@ -80,11 +82,12 @@ def test_random_tma_launch(ora, seed):
 def test_random_tma_launch_wide_rows(ora, seed):
     """Local-rank launches whose gradient rows sit 2^28 elements apart (a 3.5 GiB span
     over the eight rows): the library stages their step chunks in interleaved
-    quarter-chunk copies, the form the 7B step runs."""
-    _check_random_launch(ora, seed, True, row_numel=1 << 28)
+    quarter-chunk copies, the form the 7B step runs. Every element of every unit is
+    compared with the oracle."""
+    _check_random_launch(ora, seed, True, row_numel=1 << 28, every_element=True)
 
 
-def _check_random_launch(ora, seed, local, row_numel=0):
+def _check_random_launch(ora, seed, local, row_numel=0, every_element=False):
     torch = gu.torch()
     rng = np.random.default_rng(900 + seed)
     sms = torch.cuda.get_device_properties(0).multi_processor_count
@@ -99,10 +102,20 @@ def _check_random_launch(ora, seed, local, row_numel=0):
     else:
         units, info, bufs = bench.build_all_ranks(wl, W, torch, fs, synth)
         rb, re = 0, W
-    launches, tma = fs.fsdp_shard_step_grouped_plan(units, rb, re)
+    launches, tma, interleaved = fs.fsdp_shard_step_grouped_plan(units, rb, re, interleaved=True)
     assert tma >= 1, (launches, tma)
+    assert interleaved == (tma if row_numel >= (1 << 28) else 0), (launches, tma, interleaved)
     fs.fsdp_shard_step_grouped(units, rb, re, fs.AdamHyper(step=step, **hp))
     torch.cuda.synchronize()
+    if every_element:
+        for u, unit in enumerate(units):
+            lay = unit["layout"]
+            regen = full_parity.state_regen(wl, u, lay.numel)(lay.shard_numel)
+            assert full_parity.check_unit_every_element(
+                ora, unit, rb, re, step, regen, "seed %d unit %d" % (seed, u), hp=hp) == lay.shard_numel
+        del units, bufs
+        torch.cuda.empty_cache()
+        return
 
     def oracle(rows, master, m, v):
         g = ora.fold_mean(rows)
