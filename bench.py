@@ -416,6 +416,9 @@ def run_ours(args):
     l2 = float(getattr(torch.cuda.get_device_properties(local_rank), "L2_cache_size", 0) or 129e6)
     line = bench_line(info, workload_name, world, args.steps, args.warmup, ms_per_step, local_ms,
                       launches_per_step, tma_launches, l2, clk)
+    if ms_per_step < 1.0 and launches_per_step == 1:
+        # short steps: where host cost per call can matter, report it apart from the device time
+        line["host_us"] = host_breakdown(torch, fs, batch, rb, re, stream)
     if not args.no_e2e and name == "llama7b" and not args.units:
         line["e2e"] = e2e_local_rank(args, torch, fs, synth, wls.LLAMA7B, units, info, bufs, rb, stream,
                                      nproc, dist)
@@ -429,6 +432,55 @@ def run_ours(args):
         dist.destroy_process_group()
     if rank == 0:
         print(json.dumps(line), flush=True)
+
+
+def host_breakdown(torch, fs, batch, rb, re, stream, reps=200, graph_launches=20):
+    """Per-call cost of fsdp_shard_step_grouped, host and device apart (microseconds):
+    `binding`: the Python call (marshalling + the library call), `library`: the C call
+    made directly through ctypes less a bare ctypes call of the same signature
+    (validation, descriptor tables and the kernel launch), `ctypes_call`: that bare call
+    (zero units: it returns after checking its arguments), `device_per_launch`: one
+    launch's device time, from a CUDA graph of `graph_launches` launches replayed
+    (no host work between them)."""
+    import ctypes
+    hp = fs.AdamHyper(step=1)
+    st = stream.cuda_stream
+    lib = fs._lib
+
+    def per_call(fn):
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for _ in range(reps):
+            fn()
+        dt = (time.perf_counter() - t0) / reps
+        torch.cuda.synchronize()
+        return dt * 1e6
+
+    binding = per_call(lambda: fs.fsdp_shard_step_grouped(batch, rb, re, hp, stream=stream))
+    args = (batch.array, batch.n, rb, re, ctypes.byref(hp), st)
+    direct = per_call(lambda: lib.fsdp_shard_step_grouped(*args))
+    bare_args = (batch.array, 0, rb, re, ctypes.byref(hp), st)
+    bare = per_call(lambda: lib.fsdp_shard_step_grouped(*bare_args))
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        for _ in range(graph_launches):
+            fs.fsdp_shard_step_grouped(batch, rb, re, hp, stream=stream)
+    g.replay()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    replays = 10
+    stream.record_event(a)
+    with torch.cuda.stream(stream):
+        for _ in range(replays):
+            g.replay()
+    stream.record_event(b)
+    torch.cuda.synchronize()
+    device = a.elapsed_time(b) * 1e3 / (replays * graph_launches)
+    del g
+    return {"binding": round(binding, 2), "library": round(direct - bare, 2), "ctypes_call": round(bare, 2),
+            "device_per_launch": round(device, 2), "calls": reps,
+            "note": "host: back-to-back calls with the device keeping up; device: a CUDA graph of %d "
+                    "launches replayed %d times" % (graph_launches, replays)}
 
 
 def pipeline_setup(torch, fs, units, info, rank, n_slots):
@@ -581,9 +633,10 @@ def host_link_both_ways(torch, h2d, d2h, nbytes=3 << 30, reps=3):
 
 def run_unfused(args):
     """The step's parts as separate calls, timed on the Llama block (W = 8, all ranks):
-    per rank fsdp_reduce_scatter (fp32 gradient shard out) and fsdp_adam_shard_step
-    (bf16 shard out), then fsdp_all_gather of the 8 shards; against the fused step on
-    the same buffers. Also fsdp_pack_flat of the block's nine fp32 tensors."""
+    fsdp_reduce_scatter_ranks (every rank's fp32 gradient shard, one launch),
+    fsdp_adam_shard_step_grouped (every rank's Adam with its bf16 shard, one launch) and
+    fsdp_all_gather of the 8 shards, and the same parts one rank per launch; against the
+    fused step on the same buffers. Also fsdp_pack_flat of the block's nine fp32 tensors."""
     import torch
     import fully_sharded_gb300 as fs
     import synth
@@ -613,14 +666,23 @@ def run_unfused(args):
         return a.elapsed_time(b) / reps
 
     hp = fs.AdamHyper(step=1)
-    rs = lambda: [fs.fsdp_reduce_scatter(u["grads"], lay, r, gshard[r], stream=stream) for r in range(W)]  # noqa
-    ad = lambda: [fs.fsdp_adam_shard_step(u["master"][r], u["exp_avg"][r], u["exp_avg_sq"][r], gshard[r], hp,  # noqa
-                                          bshard[r], stream=stream) for r in range(W)]
+    # one launch per part: every rank's reduce-scatter, every rank's Adam, the gather
+    rs = lambda: fs.fsdp_reduce_scatter_ranks(u["grads"], lay, 0, W, [gshard[r] for r in range(W)],  # noqa
+                                              stream=stream)
+    adam_batch = fs.AdamShardBatch([dict(master=u["master"][r], exp_avg=u["exp_avg"][r],
+                                         exp_avg_sq=u["exp_avg_sq"][r], grad_shard=gshard[r],
+                                         bf16_shard_out=bshard[r]) for r in range(W)])
+    ad = lambda: fs.fsdp_adam_shard_step_grouped(adam_batch, hp, stream=stream)  # noqa
     ag = lambda: fs.fsdp_all_gather([bshard[r] for r in range(W)], lay, full, stream=stream)  # noqa
+    # the same parts one rank per launch (8 + 8 + 1 launches)
+    rs1 = lambda: [fs.fsdp_reduce_scatter(u["grads"], lay, r, gshard[r], stream=stream) for r in range(W)]  # noqa
+    ad1 = lambda: [fs.fsdp_adam_shard_step(u["master"][r], u["exp_avg"][r], u["exp_avg_sq"][r], gshard[r],  # noqa
+                                           hp, bshard[r], stream=stream) for r in range(W)]
     batch = fs.UnitBatch(units)
     fused = lambda: fs.fsdp_shard_step_grouped(batch, 0, W, hp, stream=stream)  # noqa
     n = args.steps
     t_rs, t_ad, t_ag, t_fused = timed(rs, n), timed(ad, n), timed(ag, n), timed(fused, n)
+    t_rs1, t_ad1 = timed(rs1, n), timed(ad1, n)
     b_rs, b_ad, b_ag = (2 * W + 4) * padded, (4 + 24 + 2) * padded, 4 * padded
     # a2: pack the nine fp32 tensors of the block into the flat master
     numels = wls.numels(wl.units[0])
@@ -634,8 +696,12 @@ def run_unfused(args):
     oracle_base = None if args.no_cpu_baseline else oracle_parts_baseline(W, 1 << 17)
     print(json.dumps({
         "workload": "llama_block_all_ranks_unfused", "W": W, "padded_elems": padded,
-        "reduce_scatter_x8": row(t_rs, b_rs), "adam_shard_step_x8": row(t_ad, b_ad), "all_gather": row(t_ag, b_ag),
-        "unfused_total": row(t_rs + t_ad + t_ag, b_rs + b_ad + b_ag),
+        "reduce_scatter_ranks": row(t_rs, b_rs), "adam_shard_step_grouped": row(t_ad, b_ad),
+        "all_gather": row(t_ag, b_ag),
+        "unfused_total": row(t_rs + t_ad + t_ag, b_rs + b_ad + b_ag), "unfused_launches": 3,
+        "per_rank_launches": {"reduce_scatter_x8": row(t_rs1, b_rs), "adam_shard_step_x8": row(t_ad1, b_ad),
+                              "unfused_total": row(t_rs1 + t_ad1 + t_ag, b_rs + b_ad + b_ag),
+                              "unfused_launches": 2 * W + 1},
         "fused": row(t_fused, (2 * W + 26) * padded),
         "fused_speedup": round((t_rs + t_ad + t_ag) / t_fused, 3),
         "pack_f32": row(t_pack, 8 * lay2.numel),

@@ -26,7 +26,8 @@ __all__ = [
     "fsdp_shard_step_grouped_launches", "fsdp_pipeline_step", "PipelineUnit", "PipelineBatch",
     "fsdp_pipeline_step_noalloc", "fsdp_all_gather_state", "fsdp_zero1_step", "fsdp_account_zero",
     "fsdp_shard_step_grouped_plan", "fsdp_device_status", "fsdp_selftest_wait_timeout",
-    "fsdp_offload_step", "OffloadUnit", "OffloadBatch",
+    "fsdp_offload_step", "OffloadUnit", "OffloadBatch", "fsdp_reduce_scatter_ranks",
+    "fsdp_adam_shard_step_grouped", "AdamShard",
 ]
 
 FSDP_OK = 0
@@ -77,6 +78,11 @@ class OffloadUnit(ctypes.Structure):
                 ("exp_avg_sq", _c_p), ("other_shards", _c_p), ("full_out", _c_p)]
 
 
+class AdamShard(ctypes.Structure):
+    _fields_ = [("master", _c_p), ("exp_avg", _c_p), ("exp_avg_sq", _c_p), ("grad_shard", _c_p),
+                ("bf16_shard_out", _c_p), ("n", _c_i64)]
+
+
 class ZeroAccount(ctypes.Structure):
     _fields_ = [(n, _c_dbl) for n in ("weights_bytes", "grads_bytes", "optimizer_bytes", "total_bytes",
                                       "reduction_vs_ddp", "comm_elems")]
@@ -118,6 +124,8 @@ def _load():
         "fsdp_unpack_flat": [P, ctypes.POINTER(Layout), P, _c_i32, P, P],
         "fsdp_reduce_scatter": [P, ctypes.POINTER(Layout), _c_i32, P, P],
         "fsdp_adam_shard_step": [P, P, P, P, _c_i64, ctypes.POINTER(AdamHyper), P, P],
+        "fsdp_reduce_scatter_ranks": [P, ctypes.POINTER(Layout), _c_i32, _c_i32, P, P],
+        "fsdp_adam_shard_step_grouped": [ctypes.POINTER(AdamShard), _c_i32, ctypes.POINTER(AdamHyper), P],
         "fsdp_all_gather": [P, ctypes.POINTER(Layout), P, P],
         "fsdp_shard_step": [P, ctypes.POINTER(Layout), _c_i32, _c_i32, P, P, P, P, P,
                             ctypes.POINTER(AdamHyper), P],
@@ -249,6 +257,39 @@ def fsdp_adam_shard_step(master, exp_avg, exp_avg_sq, grad_shard, adam: AdamHype
     _check("fsdp_adam_shard_step", _lib.fsdp_adam_shard_step(
         _dptr(master, 4), _dptr(exp_avg, 4), _dptr(exp_avg_sq, 4), _dptr(grad_shard, 4), n,
         ctypes.byref(adam), _dptr(bf16_shard_out, 2), _stream(stream)))
+
+
+def fsdp_reduce_scatter_ranks(grads, layout: Layout, rank_begin: int, rank_end: int, grad_shards_out,
+                              stream=None):
+    """a3 for ranks [rank_begin, rank_end) in one launch: grad_shards_out[r - rank_begin] (fp32 [S])
+    receives rank r's reduce-scatter."""
+    _check("fsdp_reduce_scatter_ranks", _lib.fsdp_reduce_scatter_ranks(
+        _parray(grads, 2), ctypes.byref(layout), rank_begin, rank_end, _parray(grad_shards_out, 4),
+        _stream(stream)))
+
+
+class AdamShardBatch:
+    """Marshalled shards for fsdp_adam_shard_step_grouped."""
+
+    def __init__(self, shards):
+        self.n = len(shards)
+        self.array = (AdamShard * max(1, self.n))()
+        for i, s in enumerate(shards):
+            a = self.array[i]
+            a.master = _dptr(s["master"], 4)
+            a.exp_avg = _dptr(s["exp_avg"], 4)
+            a.exp_avg_sq = _dptr(s["exp_avg_sq"], 4)
+            a.grad_shard = _dptr(s["grad_shard"], 4)
+            a.bf16_shard_out = _dptr(s.get("bf16_shard_out"), 2)
+            a.n = s["n"] if "n" in s else s["master"].numel()
+
+
+def fsdp_adam_shard_step_grouped(shards, adam: AdamHyper, stream=None):
+    """a4+a5 over several shards in one launch. `shards`: dicts (master, exp_avg, exp_avg_sq,
+    grad_shard, optional bf16_shard_out and n) or a prepared AdamShardBatch."""
+    batch = shards if isinstance(shards, AdamShardBatch) else AdamShardBatch(shards)
+    _check("fsdp_adam_shard_step_grouped", _lib.fsdp_adam_shard_step_grouped(
+        batch.array, batch.n, ctypes.byref(adam), _stream(stream)))
 
 
 def fsdp_all_gather(shards, layout: Layout, full_out, stream=None):

@@ -30,8 +30,12 @@ namespace {
 // ------------------------------------------------------------ device facts
 
 constexpr int kMaxDevices = 64;
-constexpr int kNumVariants = 7;  // W = 1, 2, 4, 8, 16, generic; 6 = the TMA form (W = 8)
+// Kernel variants: 0..5 the LDG form for W = 1, 2, 4, 8, 16 and any W with the
+// 8-consecutive-element mapping, 6 the TMA form (W = 8), 7..12 the LDG form
+// again with the split mapping (Map<true> in segment_kernel.cuh).
 constexpr int kTmaVariant = 6;
+constexpr int kSplitVariants = 7;
+constexpr int kNumVariants = 13;
 
 std::atomic<int> g_sm_count[kMaxDevices];
 std::atomic<int> g_blocks_per_sm[kMaxDevices][kNumVariants];
@@ -47,16 +51,21 @@ int variant_of(int w) {
   }
 }
 
-const void* kernel_of(int variant) {
+template <bool kSplit>
+const void* ldg_kernel_of(int variant) {
   switch (variant) {
-    case 0: return reinterpret_cast<const void*>(&segment_kernel<1>);
-    case 1: return reinterpret_cast<const void*>(&segment_kernel<2>);
-    case 2: return reinterpret_cast<const void*>(&segment_kernel<4>);
-    case 3: return reinterpret_cast<const void*>(&segment_kernel<8>);
-    case 4: return reinterpret_cast<const void*>(&segment_kernel<16>);
-    case kTmaVariant: return reinterpret_cast<const void*>(&tma_kernel<8, false>);
-    default: return reinterpret_cast<const void*>(&segment_kernel<0>);
+    case 0: return reinterpret_cast<const void*>(&segment_kernel<1, kSplit>);
+    case 1: return reinterpret_cast<const void*>(&segment_kernel<2, kSplit>);
+    case 2: return reinterpret_cast<const void*>(&segment_kernel<4, kSplit>);
+    case 3: return reinterpret_cast<const void*>(&segment_kernel<8, kSplit>);
+    case 4: return reinterpret_cast<const void*>(&segment_kernel<16, kSplit>);
+    default: return reinterpret_cast<const void*>(&segment_kernel<0, kSplit>);
   }
+}
+
+const void* kernel_of(int variant) {
+  if (variant == kTmaVariant) return reinterpret_cast<const void*>(&tma_kernel<8, false>);
+  return variant >= kSplitVariants ? ldg_kernel_of<true>(variant - kSplitVariants) : ldg_kernel_of<false>(variant);
 }
 
 // Resident-grid size for a kernel variant on the current device (cached).
@@ -93,7 +102,8 @@ int grid_capacity(int variant, int* err) {
       *err = FSDP_ECUDA;
       return 0;
     }
-    if (variant < 5 && per_sm > kBlocksPerSm) per_sm = kBlocksPerSm;
+    const int w_variant = variant >= kSplitVariants ? variant - kSplitVariants : variant;
+    if (!tma && w_variant < 5 && per_sm > kBlocksPerSm) per_sm = kBlocksPerSm;
     g_blocks_per_sm[dev][variant].store(per_sm, std::memory_order_relaxed);
   }
   return sms * per_sm;
@@ -109,7 +119,7 @@ int64_t chunks_of(const Seg& d) {
 // 1e7-element step 66.3 -> 64.5 us, 7B local-rank step 8.64 -> 8.57 ms); the
 // kernel's griddepcontrol.wait keeps every memory access after the previous
 // kernel has completed.
-template <int W>
+template <int W, bool kSplit>
 cudaError_t launch_variant(const Params& p, int grid, cudaStream_t stream) {
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3(grid);
@@ -121,7 +131,7 @@ cudaError_t launch_variant(const Params& p, int grid, cudaStream_t stream) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  const cudaError_t e = cudaLaunchKernelEx(&cfg, segment_kernel<W>, p);
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, segment_kernel<W, kSplit>, p);
   return e != cudaSuccess ? e : cudaGetLastError();
 }
 
@@ -185,6 +195,27 @@ bool use_tma(const Params& p, int tma_grid) {
 // keeps the one-copy form there.
 constexpr uintptr_t kInterleaveSpread = uintptr_t(3) << 30;
 
+// The split element mapping (Map<true>) for LDG launches whose elementwise
+// traffic is mostly fp32 state: Adam segments, and step segments whose replicas'
+// state (24 bytes per element each) is at least six times their W bf16
+// gradient rows (2 bytes each), i.e. 2 nrep >= W. Reduce segments (W rows in,
+// 4 bytes out) keep the other mapping, and so does any launch holding one.
+bool wants_split(const Params& p) {
+  bool any = false;
+  for (int k = 0; k < p.nseg; ++k) {
+    const Seg& d = p.seg[k];
+    if (d.kind == kAdam) {
+      any = true;
+    } else if (d.kind == kStep) {
+      if (2 * d.nrep < p.s.w) return false;
+      any = true;
+    } else if (d.kind == kReduce) {
+      return false;
+    }
+  }
+  return any;
+}
+
 bool wants_interleave(const Params& p) {
   for (int k = 0; k < p.nseg; ++k) {
     const Seg& d = p.seg[k];
@@ -210,8 +241,6 @@ int launch(const SegmentList& list, const Scalars& s, cudaStream_t stream, int* 
   if (list.seg.empty()) return FSDP_OK;
   const int variant = variant_of(s.w);
   int err = FSDP_OK;
-  const int cap = count ? 1 : grid_capacity(variant, &err);
-  if (err != FSDP_OK) return err;
   // the TMA form's grid: one block per SM (its pipeline fills 224 KB of shared memory)
   int tma_cap = 0;
   if (count) {
@@ -260,15 +289,24 @@ int launch(const SegmentList& list, const Scalars& s, cudaStream_t stream, int* 
         return FSDP_ECUDA;
       continue;
     }
+    const bool split = wants_split(p);
+    const int cap = grid_capacity(split ? variant + kSplitVariants : variant, &err);
+    if (err != FSDP_OK) return err;
     const int grid = static_cast<int>(std::min<int64_t>(chunks, cap));
     cudaError_t e;
-    switch (variant) {
-      case 0: e = launch_variant<1>(p, grid, stream); break;
-      case 1: e = launch_variant<2>(p, grid, stream); break;
-      case 2: e = launch_variant<4>(p, grid, stream); break;
-      case 3: e = launch_variant<8>(p, grid, stream); break;
-      case 4: e = launch_variant<16>(p, grid, stream); break;
-      default: e = launch_variant<0>(p, grid, stream); break;
+    switch (variant * 2 + (split ? 1 : 0)) {
+      case 0: e = launch_variant<1, false>(p, grid, stream); break;
+      case 1: e = launch_variant<1, true>(p, grid, stream); break;
+      case 2: e = launch_variant<2, false>(p, grid, stream); break;
+      case 3: e = launch_variant<2, true>(p, grid, stream); break;
+      case 4: e = launch_variant<4, false>(p, grid, stream); break;
+      case 5: e = launch_variant<4, true>(p, grid, stream); break;
+      case 6: e = launch_variant<8, false>(p, grid, stream); break;
+      case 7: e = launch_variant<8, true>(p, grid, stream); break;
+      case 8: e = launch_variant<16, false>(p, grid, stream); break;
+      case 9: e = launch_variant<16, true>(p, grid, stream); break;
+      case 10: e = launch_variant<0, false>(p, grid, stream); break;
+      default: e = launch_variant<0, true>(p, grid, stream); break;
     }
     if (e != cudaSuccess) return FSDP_ECUDA;
   }
@@ -497,47 +535,70 @@ extern "C" int fsdp_shard_step(const uint16_t* const* grads, const fsdp_layout_t
   return fsdp_shard_step_grouped(&u, 1, rank_begin, rank_end, adam, stream);
 }
 
-extern "C" int fsdp_reduce_scatter(const uint16_t* const* grads, const fsdp_layout_t* L,
-                                   int32_t rank, float* grad_shard_out, fsdp_stream_t stream) {
-  if (!layout_ok(L) || !grads || !grad_shard_out) return FSDP_EINVAL;
+extern "C" int fsdp_reduce_scatter_ranks(const uint16_t* const* grads, const fsdp_layout_t* L,
+                                         int32_t rank_begin, int32_t rank_end, float* const* grad_shards_out,
+                                         fsdp_stream_t stream) {
+  if (!layout_ok(L) || !grads || !grad_shards_out) return FSDP_EINVAL;
   const int W = L->world_size, F = L->shard_factor;
-  if (rank < 0 || rank >= W) return FSDP_EINVAL;
+  if (rank_begin < 0 || rank_end > W || rank_begin >= rank_end) return FSDP_EINVAL;
   const int64_t S = L->shard_numel;
   if (S == 0) return FSDP_OK;
-  const int p = rank % F;
   AliasCheck alias;
-  std::vector<const void*> ptrs;
   for (int k = 0; k < W; ++k) {
     if (!grads[k]) return FSDP_EINVAL;
     alias.input(grads[k], L->padded_numel * 2);
-    ptrs.push_back(grads[k] + p * S);
   }
-  alias.output(grad_shard_out, S * 4);
-  if (!alias.ok()) return FSDP_EALIAS;
-  ptrs.push_back(grad_shard_out);
+  // one reduce segment per owned rank, in rank order
   SegmentList list;
-  list.add_elementwise(kReduce, S, 0, ptrs);
+  std::vector<const void*> ptrs;
+  for (int r = rank_begin; r < rank_end; ++r) {
+    float* out = grad_shards_out[r - rank_begin];
+    if (!out) return FSDP_EINVAL;
+    alias.output(out, S * 4);
+    const int p = r % F;
+    ptrs.clear();
+    for (int k = 0; k < W; ++k) ptrs.push_back(grads[k] + p * S);
+    ptrs.push_back(out);
+    list.add_elementwise(kReduce, S, 0, ptrs);
+  }
+  if (!alias.ok()) return FSDP_EALIAS;
   return launch(list, reduce_only_scalars(W), reinterpret_cast<cudaStream_t>(stream));
+}
+
+extern "C" int fsdp_reduce_scatter(const uint16_t* const* grads, const fsdp_layout_t* L,
+                                   int32_t rank, float* grad_shard_out, fsdp_stream_t stream) {
+  if (!grad_shard_out || rank < 0 || rank >= FSDP_MAX_WORLD) return FSDP_EINVAL;
+  return fsdp_reduce_scatter_ranks(grads, L, rank, rank + 1, &grad_shard_out, stream);
+}
+
+extern "C" int fsdp_adam_shard_step_grouped(const fsdp_adam_shard_t* shards, int32_t n_shards,
+                                            const fsdp_adam_t* adam, fsdp_stream_t stream) {
+  if (n_shards < 0 || (n_shards > 0 && !shards)) return FSDP_EINVAL;
+  Scalars s{};
+  if (int rc = make_scalars(adam, 1, &s)) return rc;
+  AliasCheck alias;
+  SegmentList list;
+  for (int32_t i = 0; i < n_shards; ++i) {
+    const fsdp_adam_shard_t& a = shards[i];
+    if (a.n < 0) return FSDP_EINVAL;
+    if (a.n == 0) continue;
+    if (!a.master || !a.exp_avg || !a.exp_avg_sq || !a.grad_shard) return FSDP_EINVAL;
+    alias.output(a.master, a.n * 4);
+    alias.output(a.exp_avg, a.n * 4);
+    alias.output(a.exp_avg_sq, a.n * 4);
+    if (a.bf16_shard_out) alias.output(a.bf16_shard_out, a.n * 2);
+    alias.input(a.grad_shard, a.n * 4);
+    list.add_elementwise(kAdam, a.n, 1, {a.grad_shard, a.master, a.exp_avg, a.exp_avg_sq, a.bf16_shard_out});
+  }
+  if (!alias.ok()) return FSDP_EALIAS;
+  return launch(list, s, reinterpret_cast<cudaStream_t>(stream));
 }
 
 extern "C" int fsdp_adam_shard_step(float* master, float* exp_avg, float* exp_avg_sq,
                                     const float* grad_shard, int64_t n, const fsdp_adam_t* adam,
                                     uint16_t* bf16_shard_out, fsdp_stream_t stream) {
-  if (n < 0) return FSDP_EINVAL;
-  Scalars s{};
-  if (int rc = make_scalars(adam, 1, &s)) return rc;
-  if (n == 0) return FSDP_OK;
-  if (!master || !exp_avg || !exp_avg_sq || !grad_shard) return FSDP_EINVAL;
-  AliasCheck alias;
-  alias.output(master, n * 4);
-  alias.output(exp_avg, n * 4);
-  alias.output(exp_avg_sq, n * 4);
-  if (bf16_shard_out) alias.output(bf16_shard_out, n * 2);
-  alias.input(grad_shard, n * 4);
-  if (!alias.ok()) return FSDP_EALIAS;
-  SegmentList list;
-  list.add_elementwise(kAdam, n, 1, {grad_shard, master, exp_avg, exp_avg_sq, bf16_shard_out});
-  return launch(list, s, reinterpret_cast<cudaStream_t>(stream));
+  const fsdp_adam_shard_t one{master, exp_avg, exp_avg_sq, grad_shard, bf16_shard_out, n};
+  return fsdp_adam_shard_step_grouped(&one, 1, adam, stream);
 }
 
 extern "C" int fsdp_all_gather(const uint16_t* const* shards, const fsdp_layout_t* L,

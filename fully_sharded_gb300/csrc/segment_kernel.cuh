@@ -35,6 +35,27 @@ namespace fsdp {
 constexpr int kThreads = 256;
 constexpr int kVec = 8;                                 // elements per thread per chunk
 constexpr int64_t kChunkElems = int64_t(kThreads) * kVec;  // 2048 elements
+constexpr int64_t kHalf = kChunkElems / 2;
+
+// Which 8 elements of a step / reduce / Adam chunk thread t takes, as two
+// groups of 4 (the arithmetic per element is the same either way):
+//   kSplit = false: 8t .. 8t+7. Each gradient row is one 16-byte load, but a
+//     warp's 16-byte fp32 access spans 1 KB at a 32-byte stride (32 half-used
+//     sectors per instruction, each sector requested twice).
+//   kSplit = true: 4t .. 4t+3 and kHalf + 4t .. kHalf + 4t+3. A warp's fp32
+//     access covers 512 contiguous bytes (16 whole sectors), at the price of
+//     two 8-byte loads per gradient row.
+// Measured on GB300 (interleaved A/B, LDG form, fraction of the copy peak):
+// the split mapping gains where fp32 state dominates the traffic (1e9 elements
+// at W = 1 / 2: 0.952 -> 0.985 / 0.984; 16 replicas at W = 16: 0.944 -> 0.980;
+// Adam alone: 0.879 -> 0.935) and loses where the gradient rows do (W = 4:
+// 0.993 -> 0.983, W = 16 with one replica: 0.989 -> 0.963), so the host picks
+// it per launch.
+template <bool kSplit>
+struct Map {
+  static constexpr int64_t kStride = kSplit ? 4 : 8;      // thread t's first element: kStride * t
+  static constexpr int64_t kSecond = kSplit ? kHalf : 4;  // its second group, relative to the first
+};
 constexpr int kCopyVecs = 4;                              // 16-byte vectors per thread per copy chunk
 constexpr int64_t kChunkBytes = int64_t(kThreads) * 16 * kCopyVecs;  // 16 KB (copy / zero)
 // Resident blocks per SM. Measured on GB300: 3 blocks of 256 threads stream
@@ -92,6 +113,12 @@ static_assert(sizeof(Params) <= 32764, "kernel parameter block too large");
 __device__ __forceinline__ uint4 ld_stream_u4(const void* p) {
   return __ldcs(reinterpret_cast<const uint4*>(p));
 }
+__device__ __forceinline__ uint2 ld_stream_u2(const void* p) {
+  return __ldcs(reinterpret_cast<const uint2*>(p));
+}
+__device__ __forceinline__ void st_stream_u2(void* p, uint2 v) {
+  __stcs(reinterpret_cast<uint2*>(p), v);
+}
 __device__ __forceinline__ float4 ld_stream_f4(const float* p) {
   return __ldcs(reinterpret_cast<const float4*>(p));
 }
@@ -148,10 +175,50 @@ __device__ __forceinline__ void add_bf16x8(float (&acc)[8], const uint4& r) {
   acc[7] = __fadd_rn(acc[7], bf16_hi(r.w));
 }
 
-// Reduced gradient of 8 consecutive elements at e: the rows of a batch (up to
-// 8) are all loaded first (independent 16-byte loads in flight), then folded
-// in rank order.
-template <int W>
+// acc[o .. o+3] += the 4 bf16 values of r (element order: r.x low, r.x high, r.y low, r.y high).
+__device__ __forceinline__ void add_bf16x4(float (&acc)[8], int o, const uint2& r) {
+  acc[o + 0] = __fadd_rn(acc[o + 0], bf16_lo(r.x));
+  acc[o + 1] = __fadd_rn(acc[o + 1], bf16_hi(r.x));
+  acc[o + 2] = __fadd_rn(acc[o + 2], bf16_lo(r.y));
+  acc[o + 3] = __fadd_rn(acc[o + 3], bf16_hi(r.y));
+}
+
+// One gradient row's contribution to a thread's 8 elements (Map<kSplit>).
+template <bool kSplit>
+struct RowLoad {
+  uint4 a;  // kSplit = false: the 8 consecutive elements
+};
+template <>
+struct RowLoad<true> {
+  uint2 a, b;  // the two groups of 4
+};
+
+template <bool kSplit>
+__device__ __forceinline__ RowLoad<kSplit> load_row(const uint16_t* row, int64_t e) {
+  RowLoad<kSplit> r;
+  if constexpr (kSplit) {
+    r.a = ld_stream_u2(row + e);
+    r.b = ld_stream_u2(row + e + kHalf);
+  } else {
+    r.a = ld_stream_u4(row + e);
+  }
+  return r;
+}
+
+template <bool kSplit>
+__device__ __forceinline__ void add_row(float (&acc)[8], const RowLoad<kSplit>& r) {
+  if constexpr (kSplit) {
+    add_bf16x4(acc, 0, r.a);
+    add_bf16x4(acc, 4, r.b);
+  } else {
+    add_bf16x8(acc, r.a);
+  }
+}
+
+// Reduced gradient of a thread's 8 elements (first group at e): the rows of a
+// batch (up to 8) are all loaded first (independent loads in flight), then
+// folded in rank order.
+template <int W, bool kSplit>
 __device__ __forceinline__ void fold8(const Params& p, const Seg& d, int64_t e, float (&g)[8]) {
 #pragma unroll
   for (int i = 0; i < 8; ++i) g[i] = 0.0f;
@@ -160,23 +227,23 @@ __device__ __forceinline__ void fold8(const Params& p, const Seg& d, int64_t e, 
     constexpr int kBatch = W < 8 ? W : 8;
 #pragma unroll
     for (int k0 = 0; k0 < W; k0 += kBatch) {
-      uint4 r[kBatch];
+      RowLoad<kSplit> r[kBatch];
 #pragma unroll
       for (int k = 0; k < kBatch; ++k)
-        r[k] = ld_stream_u4(static_cast<const uint16_t*>(p.ptr[d.ptr + k0 + k]) + e);
+        r[k] = load_row<kSplit>(static_cast<const uint16_t*>(p.ptr[d.ptr + k0 + k]), e);
 #pragma unroll
-      for (int k = 0; k < kBatch; ++k) add_bf16x8(g, r[k]);
+      for (int k = 0; k < kBatch; ++k) add_row<kSplit>(g, r[k]);
     }
   } else {
     const int w = p.s.w;
     for (int k0 = 0; k0 < w; k0 += 8) {
-      uint4 r[8];
+      RowLoad<kSplit> r[8];
 #pragma unroll
       for (int k = 0; k < 8; ++k)
-        if (k0 + k < w) r[k] = ld_stream_u4(static_cast<const uint16_t*>(p.ptr[d.ptr + k0 + k]) + e);
+        if (k0 + k < w) r[k] = load_row<kSplit>(static_cast<const uint16_t*>(p.ptr[d.ptr + k0 + k]), e);
 #pragma unroll
       for (int k = 0; k < 8; ++k)
-        if (k0 + k < w) add_bf16x8(g, r[k]);
+        if (k0 + k < w) add_row<kSplit>(g, r[k]);
     }
   }
 #pragma unroll
@@ -192,15 +259,18 @@ __device__ __forceinline__ float fold1(const Params& p, const Seg& d, int64_t i)
   return mean_of<W>(acc, p.s);
 }
 
+// A thread's state: [0..3] at elements e .. e+3, [4..7] at the second group.
 struct State8 {
   float p[8], m[8], v[8];
 };
 
+template <bool kSplit>
 __device__ __forceinline__ void load_state8(State8& st, const float* mp, const float* mm,
                                             const float* mv, int64_t e) {
-  const float4 p0 = ld_stream_f4(mp + e), p1 = ld_stream_f4(mp + e + 4);
-  const float4 m0 = ld_stream_f4(mm + e), m1 = ld_stream_f4(mm + e + 4);
-  const float4 v0 = ld_stream_f4(mv + e), v1 = ld_stream_f4(mv + e + 4);
+  constexpr int64_t o = Map<kSplit>::kSecond;
+  const float4 p0 = ld_stream_f4(mp + e), p1 = ld_stream_f4(mp + e + o);
+  const float4 m0 = ld_stream_f4(mm + e), m1 = ld_stream_f4(mm + e + o);
+  const float4 v0 = ld_stream_f4(mv + e), v1 = ld_stream_f4(mv + e + o);
   st.p[0] = p0.x; st.p[1] = p0.y; st.p[2] = p0.z; st.p[3] = p0.w;
   st.p[4] = p1.x; st.p[5] = p1.y; st.p[6] = p1.z; st.p[7] = p1.w;
   st.m[0] = m0.x; st.m[1] = m0.y; st.m[2] = m0.z; st.m[3] = m0.w;
@@ -209,22 +279,38 @@ __device__ __forceinline__ void load_state8(State8& st, const float* mp, const f
   st.v[4] = v1.x; st.v[5] = v1.y; st.v[6] = v1.z; st.v[7] = v1.w;
 }
 
+template <bool kSplit>
 __device__ __forceinline__ void store_state8(const State8& st, float* mp, float* mm, float* mv,
                                              uint16_t* out, int64_t e) {
+  constexpr int64_t o = Map<kSplit>::kSecond;
   st_stream_f4(mp + e, make_float4(st.p[0], st.p[1], st.p[2], st.p[3]));
-  st_stream_f4(mp + e + 4, make_float4(st.p[4], st.p[5], st.p[6], st.p[7]));
+  st_stream_f4(mp + e + o, make_float4(st.p[4], st.p[5], st.p[6], st.p[7]));
   st_stream_f4(mm + e, make_float4(st.m[0], st.m[1], st.m[2], st.m[3]));
-  st_stream_f4(mm + e + 4, make_float4(st.m[4], st.m[5], st.m[6], st.m[7]));
+  st_stream_f4(mm + e + o, make_float4(st.m[4], st.m[5], st.m[6], st.m[7]));
   st_stream_f4(mv + e, make_float4(st.v[0], st.v[1], st.v[2], st.v[3]));
-  st_stream_f4(mv + e + 4, make_float4(st.v[4], st.v[5], st.v[6], st.v[7]));
+  st_stream_f4(mv + e + o, make_float4(st.v[4], st.v[5], st.v[6], st.v[7]));
   if (out) {
-    uint4 o;
-    o.x = bf16x2_rn(st.p[0], st.p[1]);
-    o.y = bf16x2_rn(st.p[2], st.p[3]);
-    o.z = bf16x2_rn(st.p[4], st.p[5]);
-    o.w = bf16x2_rn(st.p[6], st.p[7]);
-    st_stream_u4(out + e, o);
+    const uint2 lo = make_uint2(bf16x2_rn(st.p[0], st.p[1]), bf16x2_rn(st.p[2], st.p[3]));
+    const uint2 hi = make_uint2(bf16x2_rn(st.p[4], st.p[5]), bf16x2_rn(st.p[6], st.p[7]));
+    if constexpr (kSplit) {
+      st_stream_u2(out + e, lo);
+      st_stream_u2(out + e + o, hi);
+    } else {
+      st_stream_u4(out + e, make_uint4(lo.x, lo.y, hi.x, hi.y));
+    }
   }
+}
+
+// First element of thread t's first group in a chunk starting at e0.
+template <bool kSplit>
+__device__ __forceinline__ int64_t group_start(int64_t e0) {
+  return e0 + int64_t(threadIdx.x) * Map<kSplit>::kStride;
+}
+
+// Both of the thread's groups lie inside the segment: the vector path applies.
+template <bool kSplit>
+__device__ __forceinline__ bool groups_inside(int64_t e, int64_t n) {
+  return e + Map<kSplit>::kSecond + 4 <= n;
 }
 
 // ------------------------------------------------------------- segment work
@@ -248,32 +334,34 @@ __device__ __forceinline__ void step_scalar(const Params& p, const Seg& d, int64
   }
 }
 
-template <int W>
+template <int W, bool kSplit>
 __device__ __forceinline__ void step_chunk(const Params& p, const Seg& d, int64_t e0) {
   const int w = W > 0 ? W : p.s.w;
   if (d.width == 16) {
-    const int64_t e = e0 + int64_t(threadIdx.x) * kVec;
-    if (e + kVec <= d.n) {
+    const int64_t e = group_start<kSplit>(e0);
+    if (groups_inside<kSplit>(e, d.n)) {
       const int b0 = d.ptr + w;
       State8 st;
       // state of the first replica is requested before the gradient fold
-      load_state8(st, static_cast<const float*>(p.ptr[b0]), static_cast<const float*>(p.ptr[b0 + 1]),
-                  static_cast<const float*>(p.ptr[b0 + 2]), e);
+      load_state8<kSplit>(st, static_cast<const float*>(p.ptr[b0]), static_cast<const float*>(p.ptr[b0 + 1]),
+                          static_cast<const float*>(p.ptr[b0 + 2]), e);
       float g[8];
-      fold8<W>(p, d, e, g);
+      fold8<W, kSplit>(p, d, e, g);
       for (int r = 0; r < d.nrep; ++r) {
         const int b = b0 + 4 * r;
         float* mp = static_cast<float*>(const_cast<void*>(p.ptr[b]));
         float* mm = static_cast<float*>(const_cast<void*>(p.ptr[b + 1]));
         float* mv = static_cast<float*>(const_cast<void*>(p.ptr[b + 2]));
         uint16_t* out = static_cast<uint16_t*>(const_cast<void*>(p.ptr[b + 3]));
-        if (r > 0) load_state8(st, mp, mm, mv, e);
+        if (r > 0) load_state8<kSplit>(st, mp, mm, mv, e);
 #pragma unroll
         for (int i = 0; i < 8; ++i) adam1(g[i], st.p[i], st.m[i], st.v[i], p.s);
-        store_state8(st, mp, mm, mv, out, e);
+        store_state8<kSplit>(st, mp, mm, mv, out, e);
       }
-    } else {
-      for (int64_t i = e; i < d.n; ++i) step_scalar<W>(p, d, i);
+    } else {  // the segment's last, partial chunk
+      constexpr int64_t o = Map<kSplit>::kSecond;
+      for (int h = 0; h < 2; ++h)
+        for (int64_t i = e + h * o; i < e + h * o + 4 && i < d.n; ++i) step_scalar<W>(p, d, i);
     }
   } else {
 #pragma unroll 1
@@ -284,19 +372,21 @@ __device__ __forceinline__ void step_chunk(const Params& p, const Seg& d, int64_
   }
 }
 
-template <int W>
+template <int W, bool kSplit>
 __device__ __forceinline__ void reduce_chunk(const Params& p, const Seg& d, int64_t e0) {
   const int w = W > 0 ? W : p.s.w;
   float* out = static_cast<float*>(const_cast<void*>(p.ptr[d.ptr + w]));
   if (d.width == 16) {
-    const int64_t e = e0 + int64_t(threadIdx.x) * kVec;
-    if (e + kVec <= d.n) {
+    constexpr int64_t o = Map<kSplit>::kSecond;
+    const int64_t e = group_start<kSplit>(e0);
+    if (groups_inside<kSplit>(e, d.n)) {
       float g[8];
-      fold8<W>(p, d, e, g);
+      fold8<W, kSplit>(p, d, e, g);
       st_stream_f4(out + e, make_float4(g[0], g[1], g[2], g[3]));
-      st_stream_f4(out + e + 4, make_float4(g[4], g[5], g[6], g[7]));
-    } else {
-      for (int64_t i = e; i < d.n; ++i) out[i] = fold1<W>(p, d, i);
+      st_stream_f4(out + e + o, make_float4(g[4], g[5], g[6], g[7]));
+    } else {  // the segment's last, partial chunk
+      for (int h = 0; h < 2; ++h)
+        for (int64_t i = e + h * o; i < e + h * o + 4 && i < d.n; ++i) out[i] = fold1<W>(p, d, i);
     }
   } else {
 #pragma unroll 1
@@ -307,6 +397,7 @@ __device__ __forceinline__ void reduce_chunk(const Params& p, const Seg& d, int6
   }
 }
 
+template <bool kSplit>
 __device__ __forceinline__ void adam_chunk(const Params& p, const Seg& d, int64_t e0) {
   const float* gp = static_cast<const float*>(p.ptr[d.ptr]);
   float* mp = static_cast<float*>(const_cast<void*>(p.ptr[d.ptr + 1]));
@@ -314,22 +405,24 @@ __device__ __forceinline__ void adam_chunk(const Params& p, const Seg& d, int64_
   float* mv = static_cast<float*>(const_cast<void*>(p.ptr[d.ptr + 3]));
   uint16_t* out = static_cast<uint16_t*>(const_cast<void*>(p.ptr[d.ptr + 4]));
   if (d.width == 16) {
-    const int64_t e = e0 + int64_t(threadIdx.x) * kVec;
-    if (e + kVec <= d.n) {
+    const int64_t e = group_start<kSplit>(e0);
+    if (groups_inside<kSplit>(e, d.n)) {
       State8 st;
-      load_state8(st, mp, mm, mv, e);
-      const float4 g0 = ld_stream_f4(gp + e), g1 = ld_stream_f4(gp + e + 4);
+      load_state8<kSplit>(st, mp, mm, mv, e);
+      const float4 g0 = ld_stream_f4(gp + e), g1 = ld_stream_f4(gp + e + Map<kSplit>::kSecond);
       const float g[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
 #pragma unroll
       for (int i = 0; i < 8; ++i) adam1(g[i], st.p[i], st.m[i], st.v[i], p.s);
-      store_state8(st, mp, mm, mv, out, e);
+      store_state8<kSplit>(st, mp, mm, mv, out, e);
       return;
     }
   }
+  // misaligned segments, and the last, partial chunk of an aligned one
   const bool vec = d.width == 16;
-  const int64_t lo = vec ? e0 + int64_t(threadIdx.x) * kVec : 0;
+  const int64_t lo = vec ? group_start<kSplit>(e0) : 0;
   for (int k = 0; k < kVec; ++k) {
-    const int64_t i = vec ? lo + k : e0 + int64_t(k) * kThreads + threadIdx.x;
+    const int64_t i = vec ? lo + (k >> 2) * Map<kSplit>::kSecond + (k & 3)
+                          : e0 + int64_t(k) * kThreads + threadIdx.x;
     if (i >= d.n) continue;
     float pv = mp[i], mvv = mm[i], vv = mv[i];
     adam1(gp[i], pv, mvv, vv, p.s);
@@ -389,7 +482,7 @@ __device__ __forceinline__ void bytes_chunk(const Params& p, const Seg& d, int64
 
 // -------------------------------------------------------------- the kernel
 
-template <int W>
+template <int W, bool kSplit>
 __global__ void __launch_bounds__(kThreads, (W > 0 ? kBlocksPerSm : 2))
     segment_kernel(const __grid_constant__ Params p) {
   // Launched with programmatic stream serialization (see abi.cu): this grid
@@ -408,9 +501,9 @@ __global__ void __launch_bounds__(kThreads, (W > 0 ? kBlocksPerSm : 2))
     const Seg& d = p.seg[s];
     const int64_t local = c - first;
     switch (d.kind) {
-      case kStep: step_chunk<W>(p, d, local * kChunkElems); break;
-      case kReduce: reduce_chunk<W>(p, d, local * kChunkElems); break;
-      case kAdam: adam_chunk(p, d, local * kChunkElems); break;
+      case kStep: step_chunk<W, kSplit>(p, d, local * kChunkElems); break;
+      case kReduce: reduce_chunk<W, kSplit>(p, d, local * kChunkElems); break;
+      case kAdam: adam_chunk<kSplit>(p, d, local * kChunkElems); break;
       case kCopy: bytes_chunk<false>(p, d, local * kChunkBytes); break;
       default: bytes_chunk<true>(p, d, local * kChunkBytes); break;
     }

@@ -160,6 +160,19 @@ int fsdp_unpack_flat(const void *flat, const fsdp_layout_t *layout, const int64_
 int fsdp_reduce_scatter(const uint16_t *const *grads, const fsdp_layout_t *layout,
                         int32_t rank, float *grad_shard_out, fsdp_stream_t stream);
 
+/* a3 for the owned ranks [rank_begin, rank_end) in one launch (the same
+ * definition and passages as fsdp_reduce_scatter; one GPU holding several
+ * ranks reduces all of their slices at once).
+ * grads: as in fsdp_reduce_scatter. grad_shards_out: rank_end - rank_begin
+ * device pointers, fp32 [S] each, indexed by r - rank_begin; rank r's output
+ * is fsdp_reduce_scatter of rank r bit for bit (ranks at the same position of
+ * different groups get identical copies). EINVAL: a bad layout or rank range,
+ * a null pointer; EALIAS: an output overlaps a gradient row or another
+ * output. */
+int fsdp_reduce_scatter_ranks(const uint16_t *const *grads, const fsdp_layout_t *layout,
+                              int32_t rank_begin, int32_t rank_end, float *const *grad_shards_out,
+                              fsdp_stream_t stream);
+
 /* a4 + a5. Adam on one shard, in place, and its bf16 cast.
  * [math] "Why FSDP exists" (fp32 master, fp32 momentum and variance) and "The
  * backward cycle" (the optimizer updates the local slice in place).
@@ -172,6 +185,27 @@ int fsdp_reduce_scatter(const uint16_t *const *grads, const fsdp_layout_t *layou
 int fsdp_adam_shard_step(float *master, float *exp_avg, float *exp_avg_sq,
                          const float *grad_shard, int64_t n, const fsdp_adam_t *adam,
                          uint16_t *bf16_shard_out, fsdp_stream_t stream);
+
+/* One shard of fsdp_adam_shard_step_grouped (same meaning as the arguments of
+ * fsdp_adam_shard_step). */
+typedef struct {
+  float *master;            /* device fp32 [n], in place */
+  float *exp_avg;           /* device fp32 [n], in place */
+  float *exp_avg_sq;        /* device fp32 [n], in place */
+  const float *grad_shard;  /* device fp32 [n], read only */
+  uint16_t *bf16_shard_out; /* device bf16 [n], or NULL */
+  int64_t n;                /* >= 0 */
+} fsdp_adam_shard_t;
+
+/* a4 + a5 over several shards (e.g. the shards of every rank a GPU holds, or
+ * of several units) in one launch, with the same definition and passages as
+ * fsdp_adam_shard_step and one set of hyper-parameters. Each shard's results
+ * equal fsdp_adam_shard_step on it bit for bit. n_shards == 0 is a no-op.
+ * EINVAL: n_shards < 0, a negative n, a null state or gradient pointer of a
+ * non-empty shard, bad hyper-parameters; EALIAS: an output overlaps a
+ * gradient or another output (of any shard). */
+int fsdp_adam_shard_step_grouped(const fsdp_adam_shard_t *shards, int32_t n_shards,
+                                 const fsdp_adam_t *adam, fsdp_stream_t stream);
 
 /* a6. All-gather (unshard) one group.
  * [math] "The forward cycle: all-gather, compute, reshard".

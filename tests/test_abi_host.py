@@ -209,6 +209,34 @@ def test_unfused_entry_points_reject_bad_arguments():
     _expect(fs.FSDP_EALIAS, fs.fsdp_all_gather, sh[:3] + [_addr(60) + 2], lay, _addr(60))
 
 
+def test_rank_range_and_grouped_parts_reject_bad_arguments():
+    W = 4
+    lay = _lay(1000, W)
+    S = lay.shard_numel
+    g = [_addr(k) for k in range(W)]
+    outs = [_addr(20 + r) for r in range(W)]
+    _expect(fs.FSDP_EINVAL, fs.fsdp_reduce_scatter_ranks, g, lay, 0, W + 1, outs + [_addr(25)])
+    _expect(fs.FSDP_EINVAL, fs.fsdp_reduce_scatter_ranks, g, lay, 2, 2, outs)
+    _expect(fs.FSDP_EINVAL, fs.fsdp_reduce_scatter_ranks, g, lay, -1, 2, outs)
+    _expect(fs.FSDP_EINVAL, fs.fsdp_reduce_scatter_ranks, g, lay, 0, 2, [outs[0], None])
+    _expect(fs.FSDP_EINVAL, fs.fsdp_reduce_scatter_ranks, g[:3] + [None], lay, 0, 2, outs[:2])
+    _expect(fs.FSDP_EALIAS, fs.fsdp_reduce_scatter_ranks, g, lay, 0, 2, [outs[0], g[2] + 64])
+    _expect(fs.FSDP_EALIAS, fs.fsdp_reduce_scatter_ranks, g, lay, 0, 2, [outs[0], outs[0] + 4 * (S - 1)])
+    a = lambda i: _addr(30 + i)  # noqa: E731
+    shard = lambda b, n=10, **k: dict(master=a(b), exp_avg=a(b + 1), exp_avg_sq=a(b + 2),  # noqa: E731
+                                      grad_shard=a(b + 3), n=n, **k)
+    grouped = fs.fsdp_adam_shard_step_grouped
+    _expect(fs.FSDP_EINVAL, grouped, [shard(0)], fs.AdamHyper(step=0))
+    _expect(fs.FSDP_EINVAL, grouped, [shard(0), shard(5, n=-1)], HP)
+    _expect(fs.FSDP_EINVAL, grouped, [shard(0), dict(shard(5), exp_avg=None)], HP)
+    _expect(fs.FSDP_EALIAS, grouped, [shard(0), dict(shard(5), master=a(0) + 36)], HP)  # state of shard 0
+    _expect(fs.FSDP_EALIAS, grouped, [shard(0), dict(shard(5), grad_shard=a(2) + 8)], HP)
+    _expect(fs.FSDP_EALIAS, grouped, [shard(0), shard(5, bf16_shard_out=a(1) + 2)], HP)
+    # empty shards and no shards are no-ops, whatever their pointers
+    grouped([dict(master=None, exp_avg=None, exp_avg_sq=None, grad_shard=None, n=0)], HP, stream=0)
+    grouped([], HP, stream=0)
+
+
 def test_pack_unpack_reject_bad_arguments():
     lay, offs = fs.fsdp_flatten_layout([10, 20, 30], 4)
     ts = [_addr(k) for k in range(3)]
