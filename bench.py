@@ -575,6 +575,8 @@ def e2e_local_rank(args, torch, fs, synth, wl, units, info, bufs, rank, stream, 
         floor2_ms = (d2h_bytes / (both / 2 * 1e9) + (h2d_bytes - d2h_bytes) / (link["h2d_GB_per_s"] * 1e9)) * 1e3
         link.update({"both_ways_GB_per_s_total": both, "floor_two_way_ms": round(floor2_ms, 2),
                      "frac_of_floor_two_way": round(floor2_ms / ms, 4)})
+        link["host_memory"] = host_memory_bandwidth(torch)
+    link["placement"] = host_placement(torch, {"grad_slices": keep[0], "shard_out": keep[1]})
     return {"value": round(whole_job_gbs(info["bytes_per_step"], nproc, ms), 2), "unit": UNIT,
             "h2d_bytes_per_step": h2d_bytes, "d2h_bytes_per_step": d2h_bytes, "ms_per_step": round(ms, 3),
             "steps": k, "blocks_ms": [round(b, 3) for b in blocks], "host_link": link,
@@ -585,7 +587,84 @@ def e2e_local_rank(args, torch, fs, synth, wl, units, info, bufs, rank, stream, 
                     "alone; host_link: pinned copy "
                     "bandwidth measured right after, floor_ms = the step's H2D bytes at the one-way "
                     "rate, floor_two_way_ms = its D2H bytes at the two-way rate (both directions "
-                    "loaded) plus the remaining H2D bytes at the one-way rate"}
+                    "loaded) plus the remaining H2D bytes at the one-way rate; host_link.placement: "
+                    "NUMA nodes, the GPU's node and the nodes of the pinned buffers' pages; "
+                    "host_link.host_memory: the host's own read, write and copy bandwidth"}
+
+
+def host_placement(torch, buffers):
+    """Where page-locked host buffers live relative to the GPU, as the OS reports it (nothing
+    is changed): the host's NUMA nodes and their CPUs, the GPU's NUMA node (sysfs, by the
+    device's PCI address) and, per buffer, the pages on each node of the mappings that hold
+    it, and their page size (/proc/self/maps and /proc/self/numa_maps). `buffers`: name ->
+    host tensor."""
+    import glob
+    out = {"numa_nodes": {}}
+    for n in sorted(glob.glob("/sys/devices/system/node/node[0-9]*")):
+        try:
+            out["numa_nodes"][os.path.basename(n)] = open(n + "/cpulist").read().strip()
+        except OSError:
+            pass
+    try:
+        p = torch.cuda.get_device_properties(torch.cuda.current_device())
+        pci = "%04x:%02x:%02x.0" % (p.pci_domain_id, p.pci_bus_id, p.pci_device_id)
+        out["gpu_pci"] = pci
+        out["gpu_numa_node"] = int(open("/sys/bus/pci/devices/%s/numa_node" % pci).read().strip())
+    except (OSError, AttributeError, ValueError, RuntimeError):
+        out["gpu_numa_node"] = None
+    try:
+        spans = []
+        for line in open("/proc/self/maps"):
+            a, b = line.split()[0].split("-")
+            spans.append((int(a, 16), int(b, 16)))
+        info = {}
+        for line in open("/proc/self/numa_maps"):
+            f = line.split()
+            info[int(f[0], 16)] = f[1:]
+        bufs = {}
+        for name, t in buffers.items():
+            lo, hi = t.data_ptr(), t.data_ptr() + t.numel() * t.element_size()
+            pages, kb, mapped = {}, set(), 0
+            for a, b in spans:
+                if b <= lo or a >= hi or a not in info:
+                    continue
+                mapped += b - a
+                for field in info[a]:
+                    k, _, v = field.partition("=")
+                    if k.startswith("N") and k[1:].isdigit():
+                        pages[k] = pages.get(k, 0) + int(v)
+                    elif k == "kernelpagesize_kB":
+                        kb.add(int(v))
+            # the counts cover the whole mappings that hold the buffer (they may hold more)
+            bufs[name] = {"mapping_pages_per_node": pages, "page_kB": sorted(kb), "bytes": hi - lo,
+                          "mapping_bytes": mapped}
+        out["buffers"] = bufs
+    except OSError as e:
+        out["buffers"] = {"unavailable": str(e)[:120]}
+    return out
+
+
+def host_memory_bandwidth(torch, nbytes=1 << 31, reps=3):
+    """The host's own memory bandwidth as this process sees it, with torch's CPU threads
+    (GB/s, best of `reps`): a read (sum of a buffer), a write (fill) and a copy (its read and
+    write bytes both counted). The copy engines' host-side traffic competes for the same
+    memory: a host-to-device copy reads it, a device-to-host copy writes it."""
+    a = torch.empty(nbytes // 4, dtype=torch.float32)
+    a.fill_(1.0)
+    b = torch.empty_like(a)
+
+    def best(fn, nb):
+        t = float("inf")
+        for _ in range(reps):
+            t0 = time.perf_counter()
+            fn()
+            t = min(t, time.perf_counter() - t0)
+        return round(nb / t / 1e9, 1)
+
+    out = {"read_GB_per_s": best(lambda: a.sum(), nbytes), "write_GB_per_s": best(lambda: b.fill_(2.0), nbytes),
+           "copy_GB_per_s": best(lambda: b.copy_(a), 2 * nbytes), "threads": torch.get_num_threads()}
+    del a, b
+    return out
 
 
 def host_link(torch, stream, nbytes=1 << 31, reps=3):
@@ -642,7 +721,9 @@ def run_unfused(args):
     import synth
     from synth import workloads as wls
     torch.cuda.set_device(0)
-    wl = wls.LLAMA_BLOCK
+    # the Llama block, or (--unfused-elems n) one FlatParameter of n elements at W = 8: a
+    # case small enough for a many-pass profile
+    wl = sweep_workload(args.unfused_elems, 8) if args.unfused_elems else wls.LLAMA_BLOCK
     W = wl.world_size
     units, info, keep = build_all_ranks(wl, W, torch, fs, synth)
     u = units[0]
@@ -695,7 +776,8 @@ def run_unfused(args):
                          "frac_of_peak": round(b / (ms * 1e-3) / 1e9 / peak, 4)}
     oracle_base = None if args.no_cpu_baseline else oracle_parts_baseline(W, 1 << 17)
     print(json.dumps({
-        "workload": "llama_block_all_ranks_unfused", "W": W, "padded_elems": padded,
+        "workload": ("sweep_%d_W8_unfused" % args.unfused_elems) if args.unfused_elems
+        else "llama_block_all_ranks_unfused", "W": W, "padded_elems": padded,
         "reduce_scatter_ranks": row(t_rs, b_rs), "adam_shard_step_grouped": row(t_ad, b_ad),
         "all_gather": row(t_ag, b_ag),
         "unfused_total": row(t_rs + t_ad + t_ag, b_rs + b_ad + b_ag), "unfused_launches": 3,
@@ -1170,6 +1252,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--ref-sample", type=int, default=1 << 21)
+    ap.add_argument("--unfused-elems", type=int, default=0,
+                    help="unfused: one FlatParameter of this many elements at W = 8 instead of the Llama block")
     args = ap.parse_args()
     if args.warmup < 3:
         raise SystemExit("at least 3 warm-up steps")

@@ -253,10 +253,13 @@ int launch(const SegmentList& list, const Scalars& s, cudaStream_t stream, int* 
     tma_cap = grid_capacity(kTmaVariant, &err);
     if (err != FSDP_OK) return err;
   }
-  static thread_local Params p;  // ~27 KB: keep it off the stack
+  // ~27 KB: kept off the stack. Entries past this launch's nseg segments and
+  // their pointers are left as earlier launches wrote them: the kernels never read
+  // them (a chunk's segment index stays below nseg), so they are not cleared
+  // (measured on GB300: clearing cost 0.17 us of a 4.65 us call).
+  static thread_local Params p;
   size_t i = 0;
   while (i < list.seg.size()) {
-    std::memset(&p, 0, sizeof(p));
     p.s = s;
     int nseg = 0, nptr = 0;
     int64_t chunks = 0;

@@ -51,6 +51,10 @@ constexpr int64_t kHalf = kChunkElems / 2;
 // Adam alone: 0.879 -> 0.935) and loses where the gradient rows do (W = 4:
 // 0.993 -> 0.983, W = 16 with one replica: 0.989 -> 0.963), so the host picks
 // it per launch.
+// The consecutive mapping's code paths (partial chunks included) are kept in the
+// form they had before the split mapping existed: the TMA form inlines them, and
+// a rewrite of just its unstaged fallbacks made the Llama block's step 0.7-0.9 %
+// slower on GB300 (interleaved A/B, against 0.1-0.2 % between identical builds).
 template <bool kSplit>
 struct Map {
   static constexpr int64_t kStride = kSplit ? 4 : 8;      // thread t's first element: kStride * t
@@ -290,13 +294,16 @@ __device__ __forceinline__ void store_state8(const State8& st, float* mp, float*
   st_stream_f4(mv + e, make_float4(st.v[0], st.v[1], st.v[2], st.v[3]));
   st_stream_f4(mv + e + o, make_float4(st.v[4], st.v[5], st.v[6], st.v[7]));
   if (out) {
-    const uint2 lo = make_uint2(bf16x2_rn(st.p[0], st.p[1]), bf16x2_rn(st.p[2], st.p[3]));
-    const uint2 hi = make_uint2(bf16x2_rn(st.p[4], st.p[5]), bf16x2_rn(st.p[6], st.p[7]));
     if constexpr (kSplit) {
-      st_stream_u2(out + e, lo);
-      st_stream_u2(out + e + o, hi);
+      st_stream_u2(out + e, make_uint2(bf16x2_rn(st.p[0], st.p[1]), bf16x2_rn(st.p[2], st.p[3])));
+      st_stream_u2(out + e + o, make_uint2(bf16x2_rn(st.p[4], st.p[5]), bf16x2_rn(st.p[6], st.p[7])));
     } else {
-      st_stream_u4(out + e, make_uint4(lo.x, lo.y, hi.x, hi.y));
+      uint4 v;
+      v.x = bf16x2_rn(st.p[0], st.p[1]);
+      v.y = bf16x2_rn(st.p[2], st.p[3]);
+      v.z = bf16x2_rn(st.p[4], st.p[5]);
+      v.w = bf16x2_rn(st.p[6], st.p[7]);
+      st_stream_u4(out + e, v);
     }
   }
 }
@@ -359,9 +366,13 @@ __device__ __forceinline__ void step_chunk(const Params& p, const Seg& d, int64_
         store_state8<kSplit>(st, mp, mm, mv, out, e);
       }
     } else {  // the segment's last, partial chunk
-      constexpr int64_t o = Map<kSplit>::kSecond;
-      for (int h = 0; h < 2; ++h)
-        for (int64_t i = e + h * o; i < e + h * o + 4 && i < d.n; ++i) step_scalar<W>(p, d, i);
+      if constexpr (kSplit) {
+        constexpr int64_t o = Map<kSplit>::kSecond;
+        for (int h = 0; h < 2; ++h)
+          for (int64_t i = e + h * o; i < e + h * o + 4 && i < d.n; ++i) step_scalar<W>(p, d, i);
+      } else {
+        for (int64_t i = e; i < d.n; ++i) step_scalar<W>(p, d, i);
+      }
     }
   } else {
 #pragma unroll 1
@@ -385,8 +396,12 @@ __device__ __forceinline__ void reduce_chunk(const Params& p, const Seg& d, int6
       st_stream_f4(out + e, make_float4(g[0], g[1], g[2], g[3]));
       st_stream_f4(out + e + o, make_float4(g[4], g[5], g[6], g[7]));
     } else {  // the segment's last, partial chunk
-      for (int h = 0; h < 2; ++h)
-        for (int64_t i = e + h * o; i < e + h * o + 4 && i < d.n; ++i) out[i] = fold1<W>(p, d, i);
+      if constexpr (kSplit) {
+        for (int h = 0; h < 2; ++h)
+          for (int64_t i = e + h * o; i < e + h * o + 4 && i < d.n; ++i) out[i] = fold1<W>(p, d, i);
+      } else {
+        for (int64_t i = e; i < d.n; ++i) out[i] = fold1<W>(p, d, i);
+      }
     }
   } else {
 #pragma unroll 1
@@ -421,7 +436,7 @@ __device__ __forceinline__ void adam_chunk(const Params& p, const Seg& d, int64_
   const bool vec = d.width == 16;
   const int64_t lo = vec ? group_start<kSplit>(e0) : 0;
   for (int k = 0; k < kVec; ++k) {
-    const int64_t i = vec ? lo + (k >> 2) * Map<kSplit>::kSecond + (k & 3)
+    const int64_t i = vec ? (kSplit ? lo + (k >> 2) * Map<kSplit>::kSecond + (k & 3) : lo + k)
                           : e0 + int64_t(k) * kThreads + threadIdx.x;
     if (i >= d.n) continue;
     float pv = mp[i], mvv = mm[i], vv = mv[i];

@@ -150,6 +150,25 @@ def test_reference_arm_prints_one_contract_line():
     assert d["e2e"] == {"value": d["value"], "unit": d["unit"], "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
 
 
+def test_reference_arm_loads_only_the_oracle():
+    """The reference arm is the oracle alone: the CUDA library's package is never imported
+    and its shared object is never mapped into the process."""
+    import os
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    probe = ("import runpy, sys\n"
+             "sys.argv = ['bench.py', '--impl', 'reference', '--steps', '1', '--warmup', '3', '--ref-sample', '4096']\n"
+             "runpy.run_path('bench.py', run_name='__main__')\n"
+             "maps = open('/proc/self/maps').read()\n"
+             "print('PACKAGE', 'fully_sharded_gb300' in sys.modules)\n"
+             "print('LIBRARY', 'libfsdp_gb300' in maps)\n"
+             "print('ORACLE', 'libfsdp_oracle' in maps)\n")
+    out = subprocess.run([sys.executable, "-c", probe], capture_output=True, text=True, timeout=300, cwd=root)
+    assert out.returncode == 0, out.stderr[-2000:]
+    assert "PACKAGE False" in out.stdout and "LIBRARY False" in out.stdout and "ORACLE True" in out.stdout
+
+
 def test_bench_refuses_a_gpu_count_it_was_not_launched_with():
     import os
     import subprocess
