@@ -439,22 +439,24 @@ def host_breakdown(torch, fs, batch, rb, re, stream, reps=200, graph_launches=20
     `binding`: the Python call (marshalling + the library call), `library`: the C call
     made directly through ctypes less a bare ctypes call of the same signature
     (validation, descriptor tables and the kernel launch), `ctypes_call`: that bare call
-    (zero units: it returns after checking its arguments), `device_per_launch`: one
-    launch's device time, from a CUDA graph of `graph_launches` launches replayed
-    (no host work between them)."""
+    (zero units: it returns after checking its arguments), each the median of `reps`
+    calls timed one at a time with the device idle before each (so that no call waits
+    for room in the launch queue), and `device_per_launch`: one launch's device time,
+    from a CUDA graph of `graph_launches` launches replayed (no host work between them)."""
     import ctypes
     hp = fs.AdamHyper(step=1)
     st = stream.cuda_stream
     lib = fs._lib
 
     def per_call(fn):
-        torch.cuda.synchronize()
-        t0 = time.perf_counter()
+        ts = []
         for _ in range(reps):
+            torch.cuda.synchronize()
+            t0 = time.perf_counter()
             fn()
-        dt = (time.perf_counter() - t0) / reps
+            ts.append(time.perf_counter() - t0)
         torch.cuda.synchronize()
-        return dt * 1e6
+        return statistics.median(ts) * 1e6
 
     binding = per_call(lambda: fs.fsdp_shard_step_grouped(batch, rb, re, hp, stream=stream))
     args = (batch.array, batch.n, rb, re, ctypes.byref(hp), st)
@@ -479,8 +481,8 @@ def host_breakdown(torch, fs, batch, rb, re, stream, reps=200, graph_launches=20
     del g
     return {"binding": round(binding, 2), "library": round(direct - bare, 2), "ctypes_call": round(bare, 2),
             "device_per_launch": round(device, 2), "calls": reps,
-            "note": "host: back-to-back calls with the device keeping up; device: a CUDA graph of %d "
-                    "launches replayed %d times" % (graph_launches, replays)}
+            "note": "host: median of %d calls, each alone with the device idle before it; device: a CUDA "
+                    "graph of %d launches replayed %d times" % (reps, graph_launches, replays)}
 
 
 def pipeline_setup(torch, fs, units, info, rank, n_slots):

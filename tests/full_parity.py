@@ -36,48 +36,51 @@ def _h32(t) -> np.ndarray:
 
 def state_regen(wl, u, P):
     """regen for the workload builders' state of unit u (bench.build_local_rank and
-    build_all_ranks): element a of rank r's slice is flat position r * S + a of each stream."""
+    build_all_ranks), bound to the unit's S and F: element a of the slice at position
+    p = r mod F is flat position p * S + a of each stream (every replica of a position
+    holds the same draws)."""
     import torch
 
     import synth
     from synth import workloads as wls
 
-    S = None
-
-    def regen(name, r, a, n):
-        t = torch.empty(n, device="cuda")
-        idx0 = r * S + a
-        if name == "master":
-            synth.fill_(t, wls.key_master(wl, u), wl.sigma_master, idx0=idx0, n_valid=P)
-        elif wl.sigma_state:
-            key = wls.key_exp_avg(wl, u) if name == "exp_avg" else wls.key_exp_avg_sq(wl, u)
-            synth.fill_(t, key, wl.sigma_state, idx0=idx0, absval=True, n_valid=P)
-        else:
-            t.zero_()
-        return t
-
-    def bind(shard_numel):
-        nonlocal S
-        S = shard_numel
+    def bind(S, F):
+        def regen(name, r, a, n):
+            t = torch.empty(n, device="cuda")
+            idx0 = (r % F) * S + a
+            if name == "master":
+                synth.fill_(t, wls.key_master(wl, u), wl.sigma_master, idx0=idx0, n_valid=P)
+            elif wl.sigma_state:
+                key = wls.key_exp_avg(wl, u) if name == "exp_avg" else wls.key_exp_avg_sq(wl, u)
+                synth.fill_(t, key, wl.sigma_state, idx0=idx0, absval=True, n_valid=P)
+            else:
+                t.zero_()
+            return t
         return regen
 
     return bind
 
 
 def check_unit_every_element(ora, unit, rank_begin, rank_end, step, regen, what, piece=1 << 20, hp=None):
-    """Compares every element a fused step wrote for one unit (F = W, owned ranks
-    [rank_begin, rank_end), group 0) with the oracle's shard_step.
+    """Compares every element a fused step wrote for one unit (owned ranks
+    [rank_begin, rank_end); F | W, R = W / F groups) with the oracle's shard_step.
 
     unit:  the device arguments of the step (layout, grads, master / exp_avg / exp_avg_sq
            per owned rank, other_shards by rank or None, full_out per group).
     regen: regen(name, r, a, n) -> a CUDA fp32 tensor holding the pre-step value of state
            `name` ("master", "exp_avg", "exp_avg_sq") of rank r at shard elements [a, a + n).
+    piece: elements per oracle call, rounded down to a multiple of R (a piece's length
+           F * n must split evenly over the W ranks; S is a multiple of R too).
     hp:    the Adam hyper-parameters of the step (lr, beta1, beta2, eps), gpu_util.HP if None.
-    Returns the number of elements compared."""
+    Returns the number of shard elements compared."""
     lay = unit["layout"]
     W, F, S = lay.world_size, lay.shard_factor, lay.shard_numel
-    assert F == W, "pieces of F = W steps only"
+    R = W // F
     owned = list(range(rank_begin, rank_end))
+    positions = sorted({r % F for r in owned})
+    groups = sorted({r // F for r in owned})
+    local = unit["other_shards"] is not None
+    piece = max(R, piece // R * R)
     hp = dict(gu.HP if hp is None else hp)
     cores = host_cores()
     batch = cores * piece  # shard elements per round of host work
@@ -85,40 +88,47 @@ def check_unit_every_element(ora, unit, rank_begin, rank_end, step, regen, what,
     with cf.ThreadPoolExecutor(max_workers=cores) as pool:
         for a0 in range(0, S, batch):
             nb = min(batch, S - a0)
-            # inputs: gradient rows at every position's slice, state drawn again, other shards
-            # (a rank's step reads only its own position's slice of the rows)
-            g = [{r: _h16(unit["grads"][k][r * S + a0:r * S + a0 + nb]) for r in owned} for k in range(W)]
+            # inputs: the gradient rows at every owned position's slice (a step reads no
+            # other slice of them), the state drawn again, the other ranks' shards
+            g = [{p: _h16(unit["grads"][k][p * S + a0:p * S + a0 + nb]) for p in positions} for k in range(W)]
             st0 = {name: [_h32(regen(name, r, a0, nb)) for r in owned]
                    for name in ("master", "exp_avg", "exp_avg_sq")}
-            oth = [None if (r in owned or unit["other_shards"] is None) else
-                   _h16(unit["other_shards"][r][a0:a0 + nb]) for r in range(W)]
+            oth = [None] * W
+            if local:
+                for grp in groups:
+                    for p in range(F):
+                        r = grp * F + p
+                        if r not in owned:
+                            oth[r] = _h16(unit["other_shards"][r][a0:a0 + nb])
             # outputs of the device step
             got = {name: [_h32(unit[name][i][a0:a0 + nb]) for i in range(len(owned))]
                    for name in ("master", "exp_avg", "exp_avg_sq")}
-            full = unit["full_out"][0]
-            got_full = [_h16(full[p * S + a0:p * S + a0 + nb]) for p in range(F)]
+            got_full = {grp: [_h16(unit["full_out"][grp][p * S + a0:p * S + a0 + nb]) for p in range(F)]
+                        for grp in groups}
 
             def oracle_piece(i0):
+                # S and the piece length are multiples of R, so every piece is one too
                 n = min(piece, nb - i0)
+                assert n % R == 0
                 rows = np.zeros((W, F * n), np.uint16)  # slices of non-owned positions stay unread
                 for k in range(W):
-                    for r in owned:
-                        rows[k, r * n:(r + 1) * n] = g[k][r][i0:i0 + n]
+                    for p in positions:
+                        rows[k, p * n:(p + 1) * n] = g[k][p][i0:i0 + n]
                 st = {name: [x[i0:i0 + n].copy() for x in st0[name]] for name in st0}
-                others = [None if o is None else o[i0:i0 + n].copy() for o in oth]
-                out = [np.zeros(F * n, np.uint16)]
+                others = [None if o is None else o[i0:i0 + n].copy() for o in oth] if local else None
+                out = [np.zeros(F * n, np.uint16) for _ in range(R)]
                 ora.shard_step(list(rows), F, rank_begin, rank_end, st["master"], st["exp_avg"],
-                               st["exp_avg_sq"], others if unit["other_shards"] is not None else None,
-                               out, step=step, **hp)
-                return i0, n, st, out[0]
+                               st["exp_avg_sq"], others, out, step=step, **hp)
+                return i0, n, st, out
 
             for i0, n, st, out in pool.map(oracle_piece, range(0, nb, piece)):
                 at = "%s, shard elements [%d, %d)" % (what, a0 + i0, a0 + i0 + n)
                 for name in ("master", "exp_avg", "exp_avg_sq"):
                     for i, r in enumerate(owned):
                         gu.assert_same_bits(got[name][i][i0:i0 + n], st[name][i], "%s rank %d %s" % (name, r, at))
-                for p in range(F):
-                    gu.assert_same_bits(got_full[p][i0:i0 + n], out[p * n:(p + 1) * n],
-                                        "full slice %d %s" % (p, at))
+                for grp in groups:
+                    for p in range(F):
+                        gu.assert_same_bits(got_full[grp][p][i0:i0 + n], out[grp][p * n:(p + 1) * n],
+                                            "full group %d slice %d %s" % (grp, p, at))
             compared += nb
     return compared

@@ -125,7 +125,7 @@ def test_sweep_1e9_w8_every_element(ora):
     assert fs.fsdp_device_status() == 0
     lay = units[0]["layout"]
     S = lay.shard_numel
-    regen = full_parity.state_regen(wl, 0, lay.numel)(S)
+    regen = full_parity.state_regen(wl, 0, lay.numel)(S, lay.shard_factor)
     done = full_parity.check_unit_every_element(ora, units[0], 0, W, 2, regen, "sweep 1e9 W=8", piece=1 << 19)
     assert done == S
     del units, keep
@@ -220,7 +220,7 @@ def test_llama7b_local_rank_every_element(ora):
     for u in (0, 1, 16, 31, 32):
         lay = units[u]["layout"]
         S = lay.shard_numel
-        regen = full_parity.state_regen(wl, u, lay.numel)(S)
+        regen = full_parity.state_regen(wl, u, lay.numel)(S, lay.shard_factor)
         done = full_parity.check_unit_every_element(ora, units[u], rank, rank + 1, 1, regen,
                                                     "llama7b unit %d" % u)
         assert done == S

@@ -181,6 +181,24 @@ def test_hybrid_all_ranks(ora, F):
     run_step_case(ora, 16, F, [16 * 3000 + 9], 0, 16, key_base=700)
 
 
+@pytest.mark.parametrize("W,F,P", [(4, 2, 4 * 5000 + 3), (4, 1, 4 * 2048 * 3 + 1), (8, 2, 8 * 3001 + 5),
+                                   (8, 1, 8 * 2048 + 7), (3, 1, 3 * 4097 + 2), (5, 1, 5 * 777),
+                                   (64, 2, 64 * 129 + 63), (2, 2, 2 * 2048 * 5)])
+def test_split_mapping_launches(ora, W, F, P):
+    """Launches the host runs with the split element mapping (2 x replicas per position
+    >= W): every fixed-W instantiation and the generic one, ragged last chunks included."""
+    assert 2 * (W // F) >= W
+    run_step_case(ora, W, F, [P], 0, W, step=3, key_base=1100 + 10 * W + F)
+
+
+@pytest.mark.parametrize("W,F", [(2, 2), (8, 2), (3, 1)])
+def test_split_mapping_state_views(ora, W, F):
+    """The split mapping on shards that are views of one flat master (misaligned ones take
+    the scalar path beside aligned ones)."""
+    P = W * 3000 + 1  # S = W * 3001 / F: odd positions of the views start off 16-byte alignment
+    run_step_case(ora, W, F, [P // 3, P - P // 3 - 5, 5], 0, W, state_views=True, key_base=1200 + W + F)
+
+
 @pytest.mark.parametrize("F,rb,re", [(4, 5, 6), (4, 4, 8), (2, 0, 3), (8, 6, 10)])
 def test_hybrid_local(ora, F, rb, re):
     run_step_case(ora, 16, F, [16 * 2500 + 1], rb, re, key_base=800 + F)

@@ -110,7 +110,7 @@ def _check_random_launch(ora, seed, local, row_numel=0, every_element=False):
     if every_element:
         for u, unit in enumerate(units):
             lay = unit["layout"]
-            regen = full_parity.state_regen(wl, u, lay.numel)(lay.shard_numel)
+            regen = full_parity.state_regen(wl, u, lay.numel)(lay.shard_numel, lay.shard_factor)
             assert full_parity.check_unit_every_element(
                 ora, unit, rb, re, step, regen, "seed %d unit %d" % (seed, u), hp=hp) == lay.shard_numel
         del units, bufs
