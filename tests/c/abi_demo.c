@@ -3,7 +3,9 @@
  *   abi_demo host  - host-only calls: layout of the tiny MLP unit, the 7B/8-GPU
  *                    accountant example, status strings, a rejected argument.
  *   abi_demo gpu   - a fused shard step (W = 4, all ranks, 3 steps) on buffers
- *                    from cudaMalloc, checked bit for bit against the C oracle.
+ *                    from cudaMalloc, then a fourth step through the one-launch
+ *                    unfused calls (every rank's reduce-scatter, every shard's
+ *                    Adam), each checked bit for bit against the C oracle.
  * Exit status 0 on success.
  */
 #include <cuda_runtime.h>
@@ -19,6 +21,10 @@ int ora_shard_step(const uint16_t *const *grads, int32_t world_size, int32_t sha
                    int64_t padded_numel, int32_t rank_begin, int32_t rank_end, float *const *master,
                    float *const *exp_avg, float *const *exp_avg_sq, const uint16_t *const *other_shards,
                    uint16_t *const *full_out, double lr, double beta1, double beta2, double eps, int64_t step);
+int ora_reduce_scatter(const uint16_t *const *grads, int32_t world_size, int32_t shard_factor, int64_t padded_numel,
+                       int32_t rank, float *out);
+void ora_adam(float *param, float *exp_avg, float *exp_avg_sq, const float *grad, int64_t n, double lr, double beta1,
+              double beta2, double eps, int64_t step, uint16_t *bf16_out);
 
 #define CHECK(c, msg)                                   \
   do {                                                  \
@@ -113,7 +119,45 @@ static int gpu_checks(void) {
   }
   cudaMemcpy(dev_full_copy, dfull, (size_t)P * 2, cudaMemcpyDeviceToHost);
   CHECK(memcmp(dev_full_copy, hfull, (size_t)P * 2) == 0, "full bf16 differs from the oracle");
-  printf("abi_demo: 3 fused steps from C match the oracle bit for bit\n");
+
+  /* step 4 through the unfused calls: one launch reduces every rank's slice, one launch
+     updates every rank's shard (with its bf16 cast) */
+  float *dgs[W], *hgs = malloc((size_t)S * 4);
+  uint16_t *dbf[W], *hbf = malloc((size_t)S * 2), *obf = malloc((size_t)S * 2);
+  for (int r = 0; r < W; ++r) {
+    CHECK(cudaMalloc((void **)&dgs[r], (size_t)S * 4) == cudaSuccess, "cudaMalloc");
+    CHECK(cudaMalloc((void **)&dbf[r], (size_t)S * 2) == cudaSuccess, "cudaMalloc");
+    for (int64_t j = 0; j < P; ++j) hg[r][j] = bf16_trunc(uniform_pm(&seed, 1e-2f));
+    cudaMemcpy(dg[r], hg[r], (size_t)P * 2, cudaMemcpyHostToDevice);
+  }
+  adam.step = 4;
+  CHECK(fsdp_reduce_scatter_ranks((const uint16_t *const *)dg, &lay, 0, W, dgs, 0) == FSDP_OK, "reduce-scatter ranks");
+  fsdp_adam_shard_t shards[W];
+  for (int r = 0; r < W; ++r) {
+    shards[r].master = dm[r];
+    shards[r].exp_avg = de[r];
+    shards[r].exp_avg_sq = dv[r];
+    shards[r].grad_shard = dgs[r];
+    shards[r].bf16_shard_out = dbf[r];
+    shards[r].n = S;
+  }
+  CHECK(fsdp_adam_shard_step_grouped(shards, W, &adam, 0) == FSDP_OK, "grouped Adam");
+  CHECK(cudaDeviceSynchronize() == cudaSuccess, "device sync");
+  for (int r = 0; r < W; ++r) {
+    CHECK(ora_reduce_scatter((const uint16_t *const *)hg, W, W, P, r, hgs) == 0, "oracle reduce-scatter");
+    cudaMemcpy(tmp, dgs[r], (size_t)S * 4, cudaMemcpyDeviceToHost);
+    CHECK(memcmp(tmp, hgs, (size_t)S * 4) == 0, "reduce-scatter of a rank differs from the oracle");
+    ora_adam(hm[r], he[r], hv[r], hgs, S, 1e-3, 0.9, 0.999, 1e-8, 4, obf);
+    cudaMemcpy(tmp, dm[r], (size_t)S * 4, cudaMemcpyDeviceToHost);
+    CHECK(memcmp(tmp, hm[r], (size_t)S * 4) == 0, "grouped Adam master differs from the oracle");
+    cudaMemcpy(tmp, de[r], (size_t)S * 4, cudaMemcpyDeviceToHost);
+    CHECK(memcmp(tmp, he[r], (size_t)S * 4) == 0, "grouped Adam exp_avg differs from the oracle");
+    cudaMemcpy(tmp, dv[r], (size_t)S * 4, cudaMemcpyDeviceToHost);
+    CHECK(memcmp(tmp, hv[r], (size_t)S * 4) == 0, "grouped Adam exp_avg_sq differs from the oracle");
+    cudaMemcpy(hbf, dbf[r], (size_t)S * 2, cudaMemcpyDeviceToHost);
+    CHECK(memcmp(hbf, obf, (size_t)S * 2) == 0, "grouped Adam bf16 differs from the oracle");
+  }
+  printf("abi_demo: 3 fused steps and 1 unfused step from C match the oracle bit for bit\n");
   return 0;
 }
 

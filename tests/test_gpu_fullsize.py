@@ -1,15 +1,16 @@
 """Full-size workloads, in the launch configuration the benchmark times.
 
-Inputs are filled on the device by the seeded generator. The headline launch
-(the Llama-7B local-rank step, which runs the TMA form with interleaved copies)
-and the 1e9-element W = 8 step on the same instantiation are compared with the
-oracle on every element of the checked units (tests/full_parity.py runs the
-oracle on all host cores). The other workloads are checked on samples: the
-host regenerates the inputs at sampled positions (first/last elements of every
-shard, chunk and tensor boundaries, random positions), the oracle computes
-those outputs one by one, and they must equal the device outputs bit for bit.
-The hybrid workload is also checked for bit-identical parameters across
-F = 1, 4, 16 on every element.
+Inputs are filled on the device by the seeded generator. Every workload of the
+benchmark's configurations is compared with the oracle on every element
+(tests/full_parity.py runs the oracle on all host cores): the Llama block and
+the GPT-2 units (TMA form), the Llama-7B local-rank headline (TMA form with
+interleaved copies; five units), the 1e9-element sweep at W = 2, 4, 8, 16 and
+the hybrid workload at F = 16 and F = 4, whose every F also gives bit-identical
+state and parameters in every replica group (so F = 1 matches too). The two
+FlatParameters of more than 2^31 elements are checked on samples: the host
+regenerates the inputs at sampled positions (around 2^30, 2^31 and the shard
+ends, and random ones), the oracle computes those outputs one by one, and they
+must equal the device outputs bit for bit.
 """
 import numpy as np
 import pytest
@@ -87,92 +88,84 @@ def check_all_ranks_unit(ora, wl, u, unit, F, before, step, seed, extra_global=(
             gu.assert_same_bits(gather(unit["full_out"][g], i), obf, "full u%d g%d" % (u, r))
 
 
+def every_element(ora, wl, units, rb, re, step, what, piece=1 << 20):
+    """full_parity.check_unit_every_element on every unit of a launch."""
+    for u, unit in enumerate(units):
+        lay = unit["layout"]
+        regen = full_parity.state_regen(wl, u, lay.numel)(lay.shard_numel, lay.shard_factor)
+        done = full_parity.check_unit_every_element(ora, unit, rb, re, step, regen, "%s unit %d" % (what, u),
+                                                    piece=piece)
+        assert done == lay.shard_numel
+
+
 def test_llama_block_all_ranks(ora):
+    """Config 2 as the benchmark launches it (TMA form, one copy per array): every element."""
     torch = gu.torch()
     wl = wls.LLAMA_BLOCK
     units, info, keep = bench.build_all_ranks(wl, wl.world_size, torch, fs, synth)
+    assert fs.fsdp_shard_step_grouped_plan(units, 0, 8, interleaved=True) == (1, 1, 0)
     fs.fsdp_shard_step_grouped(units, 0, wl.world_size, gu.adam_hyper(1))
     torch.cuda.synchronize()
-    check_all_ranks_unit(ora, wl, 0, units[0], wl.world_size, None, 1, seed=1)
+    every_element(ora, wl, units, 0, 8, 1, "llama block")
     del units, keep
 
 
 def test_gpt2_small_grouped(ora):
+    """Config 3: 13 units in one launch of the TMA form; every element of every unit."""
     torch = gu.torch()
     wl = wls.GPT2_SMALL
     units, info, keep = bench.build_all_ranks(wl, wl.world_size, torch, fs, synth)
     assert info["params"] == 124439808
-    assert fs.fsdp_shard_step_grouped_launches(units, 0, 8) == 1
+    assert fs.fsdp_shard_step_grouped_plan(units, 0, 8) == (1, 1)
     fs.fsdp_shard_step_grouped(units, 0, wl.world_size, gu.adam_hyper(1))
     torch.cuda.synchronize()
-    for u in (0, 5, 11, 12):
-        check_all_ranks_unit(ora, wl, u, units[u], wl.world_size, None, 1, seed=10 + u)
+    every_element(ora, wl, units, 0, 8, 1, "gpt2")
     del units, keep
 
 
-def test_sweep_1e9_w8_every_element(ora):
-    """One FlatParameter of 1e9 elements stepped for all 8 ranks in one launch of the TMA form
-    with interleaved copies (the gradient rows are 2 GB apart), as the size sweep times it:
-    every element of every rank's master, exp_avg, exp_avg_sq and of the full bf16 buffer
-    equals the oracle's shard_step."""
-    torch = gu.torch()
-    n, W = 1_000_000_000, 8
-    wl = bench.sweep_workload(n, W)
-    units, info, keep = bench.build_all_ranks(wl, W, torch, fs, synth)
-    assert fs.fsdp_shard_step_grouped_plan(units, 0, W, interleaved=True) == (1, 1, 1)
-    fs.fsdp_shard_step_grouped(units, 0, W, gu.adam_hyper(2))
-    torch.cuda.synchronize()
-    assert fs.fsdp_device_status() == 0
-    lay = units[0]["layout"]
-    S = lay.shard_numel
-    regen = full_parity.state_regen(wl, 0, lay.numel)(S, lay.shard_factor)
-    done = full_parity.check_unit_every_element(ora, units[0], 0, W, 2, regen, "sweep 1e9 W=8", piece=1 << 19)
-    assert done == S
-    del units, keep
-    torch.cuda.empty_cache()
-
-
-@pytest.mark.parametrize("W", [2, 4, 16])
-def test_sweep_1e9_all_ranks(ora, W):
-    """One FlatParameter of 1e9 elements stepped for all W ranks on the LDG form, as the size
-    sweep times it. Sampled outputs of every rank, plus positions around each 2 GiB boundary
-    of the flat fp32 state, equal the oracle's (W = 8 is compared on every element above)."""
+@pytest.mark.parametrize("W", [2, 4, 8, 16])
+def test_sweep_1e9_every_element(ora, W):
+    """One FlatParameter of 1e9 elements stepped for all W ranks in one launch, as the size
+    sweep times it: the LDG form at W = 2 (split mapping), 4 and 16, and at W = 8 the TMA
+    form with interleaved copies (the gradient rows are 2 GB apart). Every element of every
+    rank's master, exp_avg, exp_avg_sq and of the full bf16 buffer equals the oracle's
+    shard_step; the fp32 state of all ranks is one flat array whose 2 GiB boundaries the
+    comparison crosses."""
     torch = gu.torch()
     n = 1_000_000_000
     wl = bench.sweep_workload(n, W)
     units, info, keep = bench.build_all_ranks(wl, W, torch, fs, synth)
-    launches, tma = fs.fsdp_shard_step_grouped_plan(units, 0, W)
-    assert launches == 1 and tma == 0
+    tma = 1 if W == 8 else 0
+    assert fs.fsdp_shard_step_grouped_plan(units, 0, W, interleaved=True) == (1, tma, tma)
     fs.fsdp_shard_step_grouped(units, 0, W, gu.adam_hyper(2))
     torch.cuda.synchronize()
-    padded = units[0]["layout"].padded_numel
-    # every rank's fp32 state is a view of one flat array: flat index x is at byte 4x,
-    # so these positions sit on each 2 GiB boundary of it
-    edges = [k << 29 for k in range(1, (padded >> 29) + 1) if (k << 29) < padded]
-    check_all_ranks_unit(ora, wl, 0, units[0], W, None, 2, seed=40 + W, extra_global=edges)
     assert fs.fsdp_device_status() == 0
+    every_element(ora, wl, units, 0, W, 2, "sweep 1e9 W=%d" % W, piece=1 << 19)
     del units, keep
     torch.cuda.empty_cache()
 
 
 def test_hybrid_full_size_identical_across_F(ora):
+    """Config 4 (W = 16, one Llama block): F = 16 and F = 4 are compared with the oracle on
+    every element of every replica; every F gives bit-identical master, exp_avg, exp_avg_sq
+    and full buffers in every replica group, so F = 1 (16 replicas) equals the oracle too."""
     torch = gu.torch()
     wl = wls.HYBRID
-    ref_master = ref_full = None
+    ref = None
     for F in (16, 4, 1):
         units, info, keep = bench.build_all_ranks(wl, F, torch, fs, synth)
         fs.fsdp_shard_step_grouped(units, 0, wl.world_size, gu.adam_hyper(1))
         torch.cuda.synchronize()
         grads, st, full = keep[0]
         R = wl.world_size // F
-        if ref_master is None:
-            ref_master, ref_full = st[0][0].clone(), full[0].clone()
-            check_all_ranks_unit(ora, wl, 0, units[0], F, None, 1, seed=20)
+        if ref is None:
+            ref = [x[0].clone() for x in st] + [full[0].clone()]
+        if F in (16, 4):
+            every_element(ora, wl, units, 0, 16, 1, "hybrid F=%d" % F)
         for g in range(R):
-            assert torch.equal(st[0][g].view(torch.int32), ref_master.view(torch.int32)), "F=%d g=%d" % (F, g)
-            assert torch.equal(full[g], ref_full), "full F=%d g=%d" % (F, g)
-        if F == 4:
-            check_all_ranks_unit(ora, wl, 0, units[0], F, None, 1, seed=21)
+            for name, x, want in zip(("master", "exp_avg", "exp_avg_sq"), st, ref):
+                assert torch.equal(x[g].view(torch.int32), want.view(torch.int32)), "%s F=%d g=%d" % (name, F, g)
+            assert torch.equal(full[g], ref[3]), "full F=%d g=%d" % (F, g)
         del units, keep, grads, st, full
         torch.cuda.empty_cache()
 

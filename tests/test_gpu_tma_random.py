@@ -1,4 +1,4 @@
-"""Random launches of the TMA form against the oracle, on sampled outputs.
+"""Random launches of the TMA form against the oracle, on every element.
 
 Each case draws a set of units (from a few elements to millions; odd sizes put
 the state views and gathered shards of later units off 16-byte alignment, which
@@ -6,12 +6,11 @@ the TMA form leaves to its unstaged path), a mode (every rank stepped, or one
 rank stepped with the other ranks' shards gathered), a step counter and Adam
 hyper-parameters. Units are added until the launch holds enough chunks for the
 library to choose the TMA form (checked with the plan). Inputs are filled on
-the device by the seeded generator; the host regenerates them at sampled
-positions (the ends of every shard, chunk boundaries, random positions), the
-oracle computes those outputs, and they must equal the device's bit for bit.
-Two more local-rank cases space the gradient rows widely enough for the
-library to pick the interleaved-copy staging; those are compared on every
-element.
+the device by the seeded generator, and every output of every unit is compared
+with the oracle's shard_step bit for bit (tests/full_parity.py). Two more
+local-rank cases space the gradient rows widely enough for the library to pick
+the interleaved-copy staging, and a 45-unit launch splits over a TMA-form and
+an LDG-form descriptor table.
 """
 import numpy as np
 import pytest
@@ -34,20 +33,6 @@ def _cuda():
     torch = pytest.importorskip("torch")
     if not torch.cuda.is_available():
         pytest.skip("needs a CUDA GPU")
-
-
-def _positions(n, rng, k=48):
-    pts = set(range(min(n, 9))) | set(range(max(0, n - 9), n))
-    for b in (2047, 2048, 2049):
-        if b < n:
-            pts.add(b)
-    pts |= set(rng.integers(0, n, size=min(k, n)).tolist())
-    return np.array(sorted(pts), dtype=np.int64)
-
-
-def _gather(t, idx):
-    torch = gu.torch()
-    return gu.to_host(t[torch.from_numpy(idx).cuda()])
 
 
 def _chunks(P, local):
@@ -82,12 +67,19 @@ def test_random_tma_launch(ora, seed):
 def test_random_tma_launch_wide_rows(ora, seed):
     """Local-rank launches whose gradient rows sit 2^28 elements apart (a 3.5 GiB span
     over the eight rows): the library stages their step chunks in interleaved
-    quarter-chunk copies, the form the 7B step runs. Every element of every unit is
-    compared with the oracle."""
-    _check_random_launch(ora, seed, True, row_numel=1 << 28, every_element=True)
+    quarter-chunk copies, the form the 7B step runs."""
+    _check_random_launch(ora, seed, True, row_numel=1 << 28)
 
 
-def _check_random_launch(ora, seed, local, row_numel=0, every_element=False):
+def _every_unit(ora, wl, units, rb, re, step, hp, what):
+    for u, unit in enumerate(units):
+        lay = unit["layout"]
+        regen = full_parity.state_regen(wl, u, lay.numel)(lay.shard_numel, lay.shard_factor)
+        assert full_parity.check_unit_every_element(ora, unit, rb, re, step, regen, "%s unit %d" % (what, u),
+                                                    hp=hp) == lay.shard_numel
+
+
+def _check_random_launch(ora, seed, local, row_numel=0):
     torch = gu.torch()
     rng = np.random.default_rng(900 + seed)
     sms = torch.cuda.get_device_properties(0).multi_processor_count
@@ -107,51 +99,7 @@ def _check_random_launch(ora, seed, local, row_numel=0, every_element=False):
     assert interleaved == (tma if row_numel >= (1 << 28) else 0), (launches, tma, interleaved)
     fs.fsdp_shard_step_grouped(units, rb, re, fs.AdamHyper(step=step, **hp))
     torch.cuda.synchronize()
-    if every_element:
-        for u, unit in enumerate(units):
-            lay = unit["layout"]
-            regen = full_parity.state_regen(wl, u, lay.numel)(lay.shard_numel, lay.shard_factor)
-            assert full_parity.check_unit_every_element(
-                ora, unit, rb, re, step, regen, "seed %d unit %d" % (seed, u), hp=hp) == lay.shard_numel
-        del units, bufs
-        torch.cuda.empty_cache()
-        return
-
-    def oracle(rows, master, m, v):
-        g = ora.fold_mean(rows)
-        p, mm, vv = master.copy(), m.copy(), v.copy()
-        bf = ora.adam(p, mm, vv, g, step=step, **hp)
-        return p, mm, vv, bf
-
-    for u, unit in enumerate(units):
-        lay = unit["layout"]
-        S, P = lay.shard_numel, lay.numel
-        owned = [rank] if local else list(range(W))
-        for r in owned:
-            j = _positions(S, rng)
-            i = r * S + j
-            if local:  # the builder's gradient pool: units alternate over two sets of rows, no pad zeroing
-                rows = [synth.normal_bf16_at(wls.key_grad(wl, u % 2, k, 0), i, wl.sigma_grad) for k in range(W)]
-            else:
-                rows = [synth.normal_bf16_at(wls.key_grad(wl, u, k, 0), i, wl.sigma_grad, n_valid=P)
-                        for k in range(W)]
-            master = synth.normal_f32_at(wls.key_master(wl, u), i, wl.sigma_master, n_valid=P)
-            m = synth.normal_f32_at(wls.key_exp_avg(wl, u), i, wl.sigma_state, absval=True, n_valid=P)
-            v = synth.normal_f32_at(wls.key_exp_avg_sq(wl, u), i, wl.sigma_state, absval=True, n_valid=P)
-            op, om, ov, obf = oracle(rows, master, m, v)
-            o = 0 if local else r
-            what = "seed %d unit %d rank %d" % (seed, u, r)
-            gu.assert_same_bits(_gather(unit["master"][o], j), op, "master " + what)
-            gu.assert_same_bits(_gather(unit["exp_avg"][o], j), om, "exp_avg " + what)
-            gu.assert_same_bits(_gather(unit["exp_avg_sq"][o], j), ov, "exp_avg_sq " + what)
-            gu.assert_same_bits(_gather(unit["full_out"][0], i), obf, "bf16 " + what)
-        if local:  # the other ranks' slices of the full buffer are copies of their shards
-            for k in (0, W - 1):
-                if k == rank:
-                    continue
-                jk = _positions(S, rng, k=24)
-                want = synth.normal_bf16_at(wls.key_shard(wl, u), k * S + jk, wl.sigma_master, n_valid=P)
-                gu.assert_same_bits(_gather(unit["full_out"][0], k * S + jk), want, "gathered unit %d k %d" % (u, k))
+    _every_unit(ora, wl, units, rb, re, step, hp, "seed %d" % seed)
     del units, bufs
     torch.cuda.empty_cache()
 
@@ -159,7 +107,7 @@ def _check_random_launch(ora, seed, local, row_numel=0, every_element=False):
 def test_grouped_launch_split_over_both_forms(ora):
     """45 local-rank units of 4 M elements: the grouped step needs two descriptor tables
     (40 units of 8 segments each fit one); the first holds enough chunks for the TMA form,
-    the second (5 units) runs on the LDG form. Every unit's sampled outputs match."""
+    the second (5 units) runs on the LDG form. Every element of every unit matches."""
     torch = gu.torch()
     rng = np.random.default_rng(990)
     sizes = [4_000_000 + int(rng.integers(0, 64)) for _ in range(45)]  # odd sizes: mixed alignment
@@ -173,24 +121,6 @@ def test_grouped_launch_split_over_both_forms(ora):
         assert tma == 1
     fs.fsdp_shard_step_grouped(units, rank, rank + 1, gu.adam_hyper(step))
     torch.cuda.synchronize()
-    for u in (0, 1, 39, 40, 44):  # both sides of the split
-        unit = units[u]
-        S, P = unit["layout"].shard_numel, unit["layout"].numel
-        j = _positions(S, rng)
-        i = rank * S + j
-        rows = [synth.normal_bf16_at(wls.key_grad(wl, u % 2, k, 0), i, wl.sigma_grad) for k in range(W)]
-        master = synth.normal_f32_at(wls.key_master(wl, u), i, wl.sigma_master, n_valid=P)
-        m = synth.normal_f32_at(wls.key_exp_avg(wl, u), i, wl.sigma_state, absval=True, n_valid=P)
-        v = synth.normal_f32_at(wls.key_exp_avg_sq(wl, u), i, wl.sigma_state, absval=True, n_valid=P)
-        g = ora.fold_mean(rows)
-        op, om, ov = master.copy(), m.copy(), v.copy()
-        obf = ora.adam(op, om, ov, g, step=step, **gu.HP)
-        gu.assert_same_bits(_gather(unit["master"][0], j), op, "master unit %d" % u)
-        gu.assert_same_bits(_gather(unit["exp_avg"][0], j), om, "exp_avg unit %d" % u)
-        gu.assert_same_bits(_gather(unit["exp_avg_sq"][0], j), ov, "exp_avg_sq unit %d" % u)
-        gu.assert_same_bits(_gather(unit["full_out"][0], i), obf, "bf16 unit %d" % u)
-        jk = _positions(S, rng, k=24)
-        want = synth.normal_bf16_at(wls.key_shard(wl, u), 0 * S + jk, wl.sigma_master, n_valid=P)
-        gu.assert_same_bits(_gather(unit["full_out"][0], jk), want, "gathered unit %d" % u)
+    _every_unit(ora, wl, units, rank, rank + 1, step, gu.HP, "split launch")
     del units, bufs
     torch.cuda.empty_cache()
