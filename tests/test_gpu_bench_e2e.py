@@ -1,6 +1,7 @@
 """The bench's end-to-end measurement (the pipelined call with host buffers) on a small
-local-rank workload: the keys of its record, the bytes it counts per step, and the
-per-step distribution it reports beside the block-timed value."""
+local-rank workload: the keys of its record, the bytes it counts per step, the
+per-step distribution it reports beside the block-timed value, and the placement of
+its pinned buffers and the host memory's bandwidth recorded beside the link rates."""
 import argparse
 
 import pytest
@@ -44,4 +45,17 @@ def test_e2e_record():
     floor2 = (e["d2h_bytes_per_step"] / r_both
               + (e["h2d_bytes_per_step"] - e["d2h_bytes_per_step"]) / (link["h2d_GB_per_s"] * 1e9)) * 1e3
     assert abs(link["floor_two_way_ms"] - floor2) < 0.02
+    # where the pinned buffers live, as the OS reports it: every page of the mappings
+    # that hold them is on some NUMA node of this host, and the GPU's node is one of them
+    place = link["placement"]
+    assert place["numa_nodes"] and set(place["buffers"]) == {"grad_slices", "shard_out"}
+    for name, b in place["buffers"].items():
+        assert b["bytes"] > 0 and b["mapping_bytes"] >= b["bytes"], name
+        pages = sum(b["mapping_pages_per_node"].values())
+        assert pages * min(b["page_kB"]) * 1024 >= b["bytes"], name
+        assert all(k[1:] in {n[4:] for n in place["numa_nodes"]} for k in b["mapping_pages_per_node"]), name
+    if place["gpu_numa_node"] is not None and place["gpu_numa_node"] >= 0:
+        assert "node%d" % place["gpu_numa_node"] in place["numa_nodes"]
+    mem = link["host_memory"]
+    assert mem["read_GB_per_s"] > 0 and mem["write_GB_per_s"] > 0 and mem["copy_GB_per_s"] > 0 and mem["threads"] >= 1
     assert fs.fsdp_device_status() == 0
