@@ -318,8 +318,8 @@ def bench_line(info, workload_name, nproc, steps, warmup, ms_per_step, local_ms,
             "unit": "GB/s",
             "frac": round(achieved / peak, 4),
             "peak_source": peak_kind,
-            "kernel": ("fsdp::tma_kernel<8>" if tma_launches == launches_per_step else
-                       "fsdp::segment_kernel<%d>" % (info["W"] if info["W"] in (1, 2, 4, 8, 16) else 0)),
+            "kernel": ("fsdp::tma_kernel<%d>" % (16 if info["W"] == 16 else 8) if tma_launches == launches_per_step
+                       else "fsdp::segment_kernel<%d>" % (info["W"] if info["W"] in (1, 2, 4, 8, 16) else 0)),
             "traffic": profiled_traffic(workload_name),
         },
         "gpu_launches": launches_per_step * steps,

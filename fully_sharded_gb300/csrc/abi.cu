@@ -32,10 +32,12 @@ namespace {
 constexpr int kMaxDevices = 64;
 // Kernel variants: 0..5 the LDG form for W = 1, 2, 4, 8, 16 and any W with the
 // 8-consecutive-element mapping, 6 the TMA form (W = 8), 7..12 the LDG form
-// again with the split mapping (Map<true> in segment_kernel.cuh).
+// again with the split mapping (Map<true> in segment_kernel.cuh), 13 the TMA
+// form for W = 16.
 constexpr int kTmaVariant = 6;
 constexpr int kSplitVariants = 7;
-constexpr int kNumVariants = 13;
+constexpr int kTma16Variant = 13;
+constexpr int kNumVariants = 14;
 
 std::atomic<int> g_sm_count[kMaxDevices];
 std::atomic<int> g_blocks_per_sm[kMaxDevices][kNumVariants];
@@ -65,6 +67,7 @@ const void* ldg_kernel_of(int variant) {
 
 const void* kernel_of(int variant) {
   if (variant == kTmaVariant) return reinterpret_cast<const void*>(&tma_kernel<8, false>);
+  if (variant == kTma16Variant) return reinterpret_cast<const void*>(&tma_kernel<16, false>);
   return variant >= kSplitVariants ? ldg_kernel_of<true>(variant - kSplitVariants) : ldg_kernel_of<false>(variant);
 }
 
@@ -85,14 +88,15 @@ int grid_capacity(int variant, int* err) {
   }
   int per_sm = g_blocks_per_sm[dev][variant].load(std::memory_order_relaxed);
   if (per_sm == 0) {
-    const bool tma = variant == kTmaVariant;
-    const int smem = tma ? TmaCfg<8>::kSmemBytes : 0;
-    // both instantiations of the TMA form (one and four copies per array) get
-    // the shared memory of the pipeline
+    const bool tma = variant == kTmaVariant || variant == kTma16Variant;
+    const int smem = variant == kTma16Variant ? TmaCfg<16>::kSmemBytes : tma ? TmaCfg<8>::kSmemBytes : 0;
+    // every instantiation of the TMA form gets the shared memory of its pipeline
+    // (for W = 8 both the one-copy and the four-round one)
     if (tma && (cudaFuncSetAttribute(kernel_of(variant), cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
                     cudaSuccess ||
-                cudaFuncSetAttribute(reinterpret_cast<const void*>(&tma_kernel<8, true>),
-                                     cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)) {
+                (variant == kTmaVariant &&
+                 cudaFuncSetAttribute(reinterpret_cast<const void*>(&tma_kernel<8, true>),
+                                      cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess))) {
       *err = FSDP_ECUDA;
       return 0;
     }
@@ -103,7 +107,7 @@ int grid_capacity(int variant, int* err) {
       return 0;
     }
     const int w_variant = variant >= kSplitVariants ? variant - kSplitVariants : variant;
-    if (!tma && w_variant < 5 && per_sm > kBlocksPerSm) per_sm = kBlocksPerSm;
+    if (!tma && w_variant < 5 && per_sm > kBlocksPerSm) per_sm = kBlocksPerSm;  // fixed-W LDG variants
     g_blocks_per_sm[dev][variant].store(per_sm, std::memory_order_relaxed);
   }
   return sms * per_sm;
@@ -135,36 +139,74 @@ cudaError_t launch_variant(const Params& p, int grid, cudaStream_t stream) {
   return e != cudaSuccess ? e : cudaGetLastError();
 }
 
-cudaError_t launch_tma(const Params& p, int grid, cudaStream_t stream, bool interleave = false) {
+template <int W, bool kInterleave>
+cudaError_t launch_tma_form(const Params& p, int grid, cudaStream_t stream) {
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3(grid);
   cfg.blockDim = dim3(kTmaThreads);
-  cfg.dynamicSmemBytes = TmaCfg<8>::kSmemBytes;
+  cfg.dynamicSmemBytes = TmaCfg<W>::kSmemBytes;
   cfg.stream = stream;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  const cudaError_t e = interleave ? cudaLaunchKernelEx(&cfg, tma_kernel<8, true>, p)
-                                   : cudaLaunchKernelEx(&cfg, tma_kernel<8, false>, p);
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, tma_kernel<W, kInterleave>, p);
   return e != cudaSuccess ? e : cudaGetLastError();
 }
 
+// The W = 8 instantiations (copy-only launches take them whatever the W of the call).
+cudaError_t launch_tma(const Params& p, int grid, cudaStream_t stream, bool interleave = false) {
+  return interleave ? launch_tma_form<8, true>(p, grid, stream) : launch_tma_form<8, false>(p, grid, stream);
+}
+
+// Largest address span of one step segment's gradient rows in a launch.
+uintptr_t max_row_span(const Params& p) {
+  uintptr_t span = 0;
+  for (int k = 0; k < p.nseg; ++k) {
+    const Seg& d = p.seg[k];
+    if (d.kind != kStep) continue;
+    uintptr_t lo = UINTPTR_MAX, hi = 0;
+    for (int r = 0; r < p.s.w; ++r) {
+      const uintptr_t a = reinterpret_cast<uintptr_t>(p.ptr[d.ptr + r]);
+      lo = std::min(lo, a);
+      hi = std::max(hi, a);
+    }
+    span = std::max(span, hi - lo);
+  }
+  return span;
+}
+
+bool has_step(const Params& p) {
+  for (int k = 0; k < p.nseg; ++k)
+    if (p.seg[k].kind == kStep) return true;
+  return false;
+}
+
+// W = 16 step launches take the TMA form only when their gradient rows span
+// 16 GiB or more of addresses. Measured on GB300 (interleaved A/B, fraction of
+// the copy peak, LDG -> TMA form with two 88 KB stages): one FlatParameter of
+// 1e9 elements (rows 2 GB apart, 30 GiB span) 0.970 -> 1.004; 5e8 (15 GiB)
+// 1.001 -> 1.008; 3e8 (9 GiB) 1.006 -> 1.017; 2e8 (6 GiB) 1.011 -> 1.017; 1e8
+// (3 GiB) 1.008 -> 1.012; but the hybrid workload's Llama block at F = W = 16
+// (6.5 GiB) 1.041 -> 1.024. Span does not separate the last case from the 2e8
+// one, so the rule takes the form only where its gain is clear.
+constexpr uintptr_t kTma16Spread = uintptr_t(16) << 30;
+
 // The TMA form pays off for launches that give every block enough chunks to
 // fill its pipeline and that hold either W = 8 steps whose positions each have
-// one replica (with any copies), or only copies (with any zero fills: pack,
-// unpack, all-gather, state gather; measured on GB300, copies of 0.4-1.7 GB
-// ran 1-3.5 % faster than on the LDG form). Its producer stages only step and
-// copy chunks; a launch holding reduce or Adam segments, steps of another W or
-// replicated steps stays on the LDG form, whose 24 warps per SM carry such
-// chunks better than the TMA form's 8 consumers.
+// one replica (with any copies; W = 16 ones under the rule above), or only
+// copies (with any zero fills: pack, unpack, all-gather, state gather; measured
+// on GB300, copies of 0.4-1.7 GB ran 1-3.5 % faster than on the LDG form). Its
+// producer stages only step and copy chunks; a launch holding reduce or Adam
+// segments, steps of another W or replicated steps stays on the LDG form, whose
+// 24 warps per SM carry such chunks better than the TMA form's 8 consumers.
 bool use_tma(const Params& p, int tma_grid) {
   bool step = false, copy = false;
   for (int k = 0; k < p.nseg; ++k) {
     const Seg& d = p.seg[k];
     if (d.kind == kStep) {
-      if (d.nrep != 1 || p.s.w != 8) return false;
+      if (d.nrep != 1 || (p.s.w != 8 && p.s.w != 16)) return false;
       step = true;
     } else if (d.kind == kCopy) {
       copy = true;
@@ -175,6 +217,7 @@ bool use_tma(const Params& p, int tma_grid) {
   if (step) {
     for (int k = 0; k < p.nseg; ++k)
       if (p.seg[k].kind == kZero) return false;
+    if (p.s.w == 16 && max_row_span(p) < kTma16Spread) return false;
   } else if (!copy) {
     return false;
   }
@@ -216,20 +259,8 @@ bool wants_split(const Params& p) {
   return any;
 }
 
-bool wants_interleave(const Params& p) {
-  for (int k = 0; k < p.nseg; ++k) {
-    const Seg& d = p.seg[k];
-    if (d.kind != kStep) continue;
-    uintptr_t lo = UINTPTR_MAX, hi = 0;
-    for (int r = 0; r < p.s.w; ++r) {
-      const uintptr_t a = reinterpret_cast<uintptr_t>(p.ptr[d.ptr + r]);
-      lo = std::min(lo, a);
-      hi = std::max(hi, a);
-    }
-    if (hi - lo >= kInterleaveSpread) return true;
-  }
-  return false;
-}
+// (W = 8 launches only: the W = 16 instantiation copies one piece per array.)
+bool wants_interleave(const Params& p) { return p.s.w == 8 && max_row_span(p) >= kInterleaveSpread; }
 
 }  // namespace
 
@@ -280,10 +311,18 @@ int launch(const SegmentList& list, const Scalars& s, cudaStream_t stream, int* 
     p.wait_limit_ns = kDefaultWaitLimitNs;
     p.inject_tx = 0;
     const bool tma = use_tma(p, tma_cap);
+    const bool tma16 = tma && p.s.w == 16 && has_step(p);
     if (count) {
       ++*count;
       if (tma && tma_count) ++*tma_count;
-      if (tma && interleaved_count && wants_interleave(p)) ++*interleaved_count;
+      if (tma && !tma16 && interleaved_count && wants_interleave(p)) ++*interleaved_count;
+      continue;
+    }
+    if (tma16) {
+      const int cap16 = grid_capacity(kTma16Variant, &err);
+      if (err != FSDP_OK) return err;
+      if (launch_tma_form<16, false>(p, static_cast<int>(std::min<int64_t>(chunks, cap16)), stream) != cudaSuccess)
+        return FSDP_ECUDA;
       continue;
     }
     if (tma) {

@@ -10,18 +10,21 @@
 // cannot be staged (misaligned segments, other kinds) are run by the
 // consumers from global memory as in segment_kernel.
 //
-// Two instantiations: kInterleave = false stages a step chunk with one bulk
-// copy per array; kInterleave = true (the host picks it when a launch's
-// gradient rows span 3 GiB or more of addresses) in four rounds of quarter
-// chunks over the arrays.
+// Instantiations: for W = 8, kInterleave = false stages a step chunk with one
+// bulk copy per array and kInterleave = true (the host picks it when a
+// launch's gradient rows span 3 GiB or more of addresses) in four rounds of
+// quarter chunks over the arrays; for W = 16 (one copy per array, two stages
+// of 88 KB), the host picks it for launches whose gradient rows span 16 GiB or
+// more.
 //
 // Measured on GB300 against segment_kernel (same chunks, same arithmetic,
 // bit-identical results): W = 8 single-replica step launches gain 1-4 %
 // (Llama block 1.246 -> 1.206 ms); W <= 4, replica-heavy hybrid steps, short
 // launches and launches of reduce chunks lose, so the host uses this form only
-// for W = 8 launches made of one-replica step segments (and copies), and for
-// launches of copies only (and zero fills: pack, unpack, the gathers; 1-3.5 %
-// faster), with at least kTmaMinChunksPerBlock chunks per block.
+// for W = 8 launches made of one-replica step segments (and copies), for W = 16
+// ones whose rows span 16 GiB or more (see abi.cu), and for launches of copies
+// only (and zero fills: pack, unpack, the gathers; 1-3.5 % faster), with at
+// least kTmaMinChunksPerBlock chunks per block.
 //
 // Every mbarrier wait is bounded in time (Params::wait_limit_ns, read from
 // %globaltimer): when a wait runs out the block sets bit 0 of g_fsdp_status,
@@ -39,19 +42,21 @@ namespace fsdp {
 
 constexpr int kTmaConsumerWarps = 8;
 constexpr int kTmaThreads = (kTmaConsumerWarps + 1) * 32;
-constexpr int kTmaStages = 4;  // 4 x 56 KB at W = 8
+constexpr int kTmaStages = 4;  // 4 x 56 KB at W = 8 (W = 16: 2 x 88 KB)
 constexpr int kTmaMinChunksPerBlock = 128;
 constexpr uint64_t kDefaultWaitLimitNs = 2000000000ull;  // 2 s
 
 template <int W>
 struct TmaCfg {
+  static constexpr int kStages = W > 8 ? 2 : kTmaStages;
   static constexpr int kRowBytes = int(kChunkElems) * 2;
   static constexpr int kStateBytes = int(kChunkElems) * 4;
   static constexpr int kStepBytes = W * kRowBytes + 3 * kStateBytes;
   static constexpr int kStageBytes = kStepBytes > int(kChunkBytes) ? kStepBytes : int(kChunkBytes);
-  static constexpr int kSmemBytes = kTmaStages * kStageBytes;
+  static constexpr int kSmemBytes = kStages * kStageBytes;
 };
 static_assert(TmaCfg<8>::kSmemBytes + 128 <= 232448, "TMA pipeline exceeds 227 KB of shared memory");
+static_assert(TmaCfg<16>::kSmemBytes + 128 <= 232448, "TMA pipeline exceeds 227 KB of shared memory");
 
 struct Cursor {
   int s = 0;
@@ -258,8 +263,8 @@ __device__ __forceinline__ void tma_store_copy(const Params& p, const Seg& d, in
 template <int W, bool kInterleave>
 __global__ void __launch_bounds__(kTmaThreads, 1) tma_kernel(const __grid_constant__ Params p) {
   extern __shared__ __align__(128) unsigned char smem[];
-  __shared__ __align__(8) uint64_t full_bar[kTmaStages];
-  __shared__ __align__(8) uint64_t empty_bar[kTmaStages];
+  __shared__ __align__(8) uint64_t full_bar[TmaCfg<W>::kStages];
+  __shared__ __align__(8) uint64_t empty_bar[TmaCfg<W>::kStages];
   __shared__ int abort_store;
   volatile int* abort_flag = &abort_store;
   // programmatic dependent launch, as in segment_kernel
@@ -267,7 +272,7 @@ __global__ void __launch_bounds__(kTmaThreads, 1) tma_kernel(const __grid_consta
   asm volatile("griddepcontrol.launch_dependents;");
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   if (threadIdx.x == 0) {
-    for (int s = 0; s < kTmaStages; ++s) {
+    for (int s = 0; s < TmaCfg<W>::kStages; ++s) {
       mbar_init(sm_addr(&full_bar[s]), 1);
       mbar_init(sm_addr(&empty_bar[s]), kTmaConsumerWarps);
     }
@@ -280,13 +285,13 @@ __global__ void __launch_bounds__(kTmaThreads, 1) tma_kernel(const __grid_consta
   const uint64_t limit = p.wait_limit_ns;
   if (warp == kTmaConsumerWarps) {  // producer
     if (lane != 0) return;
-    int pending[kTmaStages];  // parity of the last issued phase of each stage, -1 if none
-    for (int s = 0; s < kTmaStages; ++s) pending[s] = -1;
+    int pending[TmaCfg<W>::kStages];  // parity of the last issued phase of each stage, -1 if none
+    for (int s = 0; s < TmaCfg<W>::kStages; ++s) pending[s] = -1;
     Cursor cur;
     uint32_t i = 0;
     for (int64_t c = blockIdx.x; c < p.total_chunks; c += G, ++i) {
-      const int stage = static_cast<int>(i % kTmaStages);
-      const uint32_t round = i / kTmaStages;
+      const int stage = static_cast<int>(i % TmaCfg<W>::kStages);
+      const uint32_t round = i / TmaCfg<W>::kStages;
       if (!wait_phase(sm_addr(&empty_bar[stage]), (round & 1u) ^ 1u, abort_flag, limit)) break;
       int64_t l, staged;
       const Seg& d = cur.at(p, c, l);
@@ -297,7 +302,7 @@ __global__ void __launch_bounds__(kTmaThreads, 1) tma_kernel(const __grid_consta
       pending[stage] = static_cast<int>(round & 1u);
     }
     {  // every issued bulk copy lands before the block can exit (bounded)
-      for (int s = 0; s < kTmaStages; ++s) {
+      for (int s = 0; s < TmaCfg<W>::kStages; ++s) {
         if (pending[s] < 0) continue;
         const uint64_t t0 = global_ns();
         while (!mbar_try_wait(sm_addr(&full_bar[s]), static_cast<uint32_t>(pending[s])) &&
@@ -310,8 +315,8 @@ __global__ void __launch_bounds__(kTmaThreads, 1) tma_kernel(const __grid_consta
   Cursor cur;  // consumers
   uint32_t i = 0;
   for (int64_t c = blockIdx.x; c < p.total_chunks; c += G, ++i) {
-    const int stage = static_cast<int>(i % kTmaStages);
-    const uint32_t round = i / kTmaStages;
+    const int stage = static_cast<int>(i % TmaCfg<W>::kStages);
+    const uint32_t round = i / TmaCfg<W>::kStages;
     if (!wait_phase(sm_addr(&full_bar[stage]), round & 1u, abort_flag, limit)) break;
     int64_t l, staged;
     const Seg& d = cur.at(p, c, l);

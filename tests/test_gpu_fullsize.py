@@ -126,8 +126,9 @@ def test_gpt2_small_grouped(ora):
 @pytest.mark.parametrize("W", [2, 4, 8, 16])
 def test_sweep_1e9_every_element(ora, W):
     """One FlatParameter of 1e9 elements stepped for all W ranks in one launch, as the size
-    sweep times it: the LDG form at W = 2 (split mapping), 4 and 16, and at W = 8 the TMA
-    form with interleaved copies (the gradient rows are 2 GB apart). Every element of every
+    sweep times it: the LDG form at W = 2 (split mapping) and 4, the TMA form with
+    interleaved copies at W = 8 and the W = 16 TMA form at W = 16 (the gradient rows are
+    2 GB apart). Every element of every
     rank's master, exp_avg, exp_avg_sq and of the full bf16 buffer equals the oracle's
     shard_step; the fp32 state of all ranks is one flat array whose 2 GiB boundaries the
     comparison crosses."""
@@ -135,8 +136,10 @@ def test_sweep_1e9_every_element(ora, W):
     n = 1_000_000_000
     wl = bench.sweep_workload(n, W)
     units, info, keep = bench.build_all_ranks(wl, W, torch, fs, synth)
-    tma = 1 if W == 8 else 0
-    assert fs.fsdp_shard_step_grouped_plan(units, 0, W, interleaved=True) == (1, tma, tma)
+    # the TMA form at W = 8 (interleaved copies: rows 3 GiB or more apart) and at W = 16 (rows
+    # spanning 16 GiB or more), the LDG form at W = 2 and 4
+    tma, interleaved = (1 if W in (8, 16) else 0), (1 if W == 8 else 0)
+    assert fs.fsdp_shard_step_grouped_plan(units, 0, W, interleaved=True) == (1, tma, interleaved)
     fs.fsdp_shard_step_grouped(units, 0, W, gu.adam_hyper(2))
     torch.cuda.synchronize()
     assert fs.fsdp_device_status() == 0
