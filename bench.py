@@ -871,6 +871,13 @@ def run_offload(args):
     # the staged step moves 12 B per shard element each way, both directions at once
     both = host_link_both_ways(torch, h2d, d2h)
     floor_ms = 12 * S_tot / (both / 2 * 1e9) * 1e3
+    # a pipeline cannot keep both directions busy from start to end: the first unit's state
+    # arrives before anything goes back, the last unit's goes back after everything came in
+    # (each at its one-way rate); the rest moves at the two-way rate
+    link1 = host_link(torch, h2d)
+    first, last = 12 * units[0]["layout"].shard_numel, 12 * units[-1]["layout"].shard_numel
+    fill_drain_ms = (first / (link1["h2d_GB_per_s"] * 1e9) + last / (link1["d2h_GB_per_s"] * 1e9)
+                     + max(12 * S_tot - first, 12 * S_tot - last) / (both / 2 * 1e9)) * 1e3
     oracle_base = None if args.no_cpu_baseline else cpu_baseline(units, info, bufs, 0, torch, seconds=3.0)
     print(json.dumps({
         "workload": "llama7b_local_rank_state_offload", "W": wl.world_size, "shard_elems": S_tot,
@@ -883,7 +890,10 @@ def run_offload(args):
                                  "host_link_GB_per_s": round(24 * S_tot / (ms_host * 1e-3) / 1e9, 1)},
         "state_in_host_memory_staged": staged,
         "host_link_both_ways": {"GB_per_s_total": both, "floor_ms": round(floor_ms, 2),
-                                "staged_frac_of_floor": round(floor_ms / best, 4)},
+                                "staged_frac_of_floor": round(floor_ms / best, 4),
+                                "one_way_GB_per_s": link1,
+                                "floor_with_fill_and_drain_ms": round(fill_drain_ms, 2),
+                                "staged_frac_of_floor_with_fill_and_drain": round(fill_drain_ms / best, 4)},
         "gpu_memory_saved_bytes": 12 * S_tot,
         "slowdown": round(ms_host / ms_hbm, 2),
         "staged_slowdown": round(best / ms_hbm, 2),
