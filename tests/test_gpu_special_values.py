@@ -1,9 +1,11 @@
 """Special values through the fused step: +-inf, NaN, subnormal and signed-zero gradients,
 huge and subnormal parameters. Non-NaN outputs must equal the oracle bit for bit; NaN must
-appear exactly where the oracle has NaN (NaN payloads are not specified). The first case
-runs on the LDG form (W = 4, one small unit); the others put the same kind of unit at W = 8
-into a grouped launch with a zero-filled unit large enough for the library to choose the
-TMA form, all ranks and one rank with its gather."""
+appear exactly where the oracle has NaN (NaN payloads are not specified). The first cases
+run on the LDG form (one small unit; W = 4 with the consecutive element mapping, and W = 2,
+and W = 4 and 16 with replicas, with the split one), then Adam alone over two shards (split
+mapping); the last put the same kind of unit at W = 8 into a grouped launch with a
+zero-filled unit large enough for the library to choose the TMA form, all ranks and one rank
+with its gather (tests/test_gpu_tma16.py does the same for the W = 16 TMA form)."""
 import numpy as np
 import pytest
 
@@ -39,12 +41,15 @@ def _same_or_both_nan_bf16(got, want, what):
     _same_or_both_nan(f(got), f(want), what)
 
 
-def test_special_values_match_oracle(ora):
+@pytest.mark.parametrize("W,F", [(4, 4), (2, 2), (4, 1), (16, 2)])
+def test_special_values_match_oracle(ora, W, F):
+    """The LDG form with the consecutive element mapping (W = 4, F = 4) and with the split
+    one (W = 2; W = 4 with four replicas per position; W = 16 with eight)."""
     torch = gu.torch()
-    W, P = 4, 4 * 4096
-    lay, _ = fs.fsdp_flatten_layout([P], W)
-    S = lay.shard_numel
-    rng = np.random.default_rng(3)
+    P = W * 4096
+    lay, _ = fs.fsdp_flatten_layout([P], W, F)
+    S, R = lay.shard_numel, W // F
+    rng = np.random.default_rng(3 + W + F)
     specials = np.array([np.inf, -np.inf, np.nan, 0.0, -0.0, 1e-40, -1e-40, 3.3e38, -3.3e38, 1e-3],
                         dtype=np.float32)
     grads = []
@@ -59,16 +64,15 @@ def test_special_values_match_oracle(ora):
     m = np.abs(synth.normal_f32(synth.stream_key(77, 2), P, 1e-4))
     v = np.abs(synth.normal_f32(synth.stream_key(77, 3), P, 1e-4))
     v[rng.choice(P, size=P // 32, replace=False)] = 0.0
-    om = [master[r * S:(r + 1) * S].copy() for r in range(W)]
-    oe = [m[r * S:(r + 1) * S].copy() for r in range(W)]
-    ov = [v[r * S:(r + 1) * S].copy() for r in range(W)]
-    ofull = [np.zeros(P, np.uint16)]
-    ora.shard_step(grads, W, 0, W, om, oe, ov, None, ofull, step=2, **gu.HP)
-    md = [gu.to_dev(master[r * S:(r + 1) * S]) for r in range(W)]
-    ed = [gu.to_dev(m[r * S:(r + 1) * S]) for r in range(W)]
-    vd = [gu.to_dev(v[r * S:(r + 1) * S]) for r in range(W)]
-    full = torch.zeros(P, dtype=torch.int16, device="cuda")
-    fs.fsdp_shard_step([gu.to_dev(g) for g in grads], lay, 0, W, md, ed, vd, None, [full], gu.adam_hyper(2))
+    sl = lambda a, r: a[(r % F) * S:(r % F + 1) * S].copy()  # noqa: E731
+    om, oe, ov = [sl(master, r) for r in range(W)], [sl(m, r) for r in range(W)], [sl(v, r) for r in range(W)]
+    ofull = [np.zeros(P, np.uint16) for _ in range(R)]
+    ora.shard_step(grads, F, 0, W, om, oe, ov, None, ofull, step=2, **gu.HP)
+    md = [gu.to_dev(sl(master, r)) for r in range(W)]
+    ed = [gu.to_dev(sl(m, r)) for r in range(W)]
+    vd = [gu.to_dev(sl(v, r)) for r in range(W)]
+    full = [torch.zeros(P, dtype=torch.int16, device="cuda") for _ in range(R)]
+    fs.fsdp_shard_step([gu.to_dev(g) for g in grads], lay, 0, W, md, ed, vd, None, full, gu.adam_hyper(2))
     torch.cuda.synchronize()
     nan_seen = 0
     for r in range(W):
@@ -76,8 +80,44 @@ def test_special_values_match_oracle(ora):
         _same_or_both_nan(gu.to_host(ed[r]), oe[r], "exp_avg r%d" % r)
         _same_or_both_nan(gu.to_host(vd[r]), ov[r], "exp_avg_sq r%d" % r)
         nan_seen += int(np.isnan(om[r]).sum())
-    _same_or_both_nan_bf16(gu.to_host(full), ofull[0], "full")
+    for g in range(R):
+        _same_or_both_nan_bf16(gu.to_host(full[g]), ofull[g], "full g%d" % g)
     assert nan_seen > 0  # the case does reach the NaN paths
+
+
+def test_special_values_grouped_adam(ora):
+    """Adam alone (split element mapping) on special gradients and masters, two shards of one
+    launch, one of them ragged."""
+    torch = gu.torch()
+    rng = np.random.default_rng(33)
+    specials = np.array([np.inf, -np.inf, np.nan, 0.0, -0.0, 1e-40, -1e-40, 3.3e38, -3.3e38, 1e-3],
+                        dtype=np.float32)
+    shards, want = [], []
+    for n in (8192, 5003):
+        g = (rng.standard_normal(n) * 1e-2).astype(np.float32)
+        idx = rng.choice(n, size=n // 16, replace=False)
+        g[idx] = rng.choice(specials, size=idx.size)
+        p = (rng.standard_normal(n) * 0.02).astype(np.float32)
+        idx = rng.choice(n, size=n // 16, replace=False)
+        p[idx] = rng.choice(np.array([0.0, -0.0, 1e-40, 3e38, -3e38, 1.0], np.float32), size=idx.size)
+        m = np.abs(rng.standard_normal(n) * 1e-4).astype(np.float32)
+        v = np.abs(rng.standard_normal(n) * 1e-4).astype(np.float32)
+        v[rng.choice(n, size=n // 32, replace=False)] = 0.0
+        op, om, ov = p.copy(), m.copy(), v.copy()
+        obf = ora.adam(op, om, ov, g, step=5, **gu.HP)
+        want.append((op, om, ov, obf))
+        shards.append(dict(master=gu.to_dev(p), exp_avg=gu.to_dev(m), exp_avg_sq=gu.to_dev(v),
+                           grad_shard=gu.to_dev(g), bf16_shard_out=torch.zeros(n, dtype=torch.int16, device="cuda")))
+    fs.fsdp_adam_shard_step_grouped(shards, gu.adam_hyper(5))
+    torch.cuda.synchronize()
+    nan_seen = 0
+    for i, (s, (op, om, ov, obf)) in enumerate(zip(shards, want)):
+        _same_or_both_nan(gu.to_host(s["master"]), op, "master %d" % i)
+        _same_or_both_nan(gu.to_host(s["exp_avg"]), om, "exp_avg %d" % i)
+        _same_or_both_nan(gu.to_host(s["exp_avg_sq"]), ov, "exp_avg_sq %d" % i)
+        _same_or_both_nan_bf16(gu.to_host(s["bf16_shard_out"]), obf, "bf16 %d" % i)
+        nan_seen += int(np.isnan(op).sum())
+    assert nan_seen > 0
 
 
 def _special_inputs(rng, W, P, padded):
