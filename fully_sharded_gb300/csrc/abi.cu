@@ -183,15 +183,30 @@ bool has_step(const Params& p) {
   return false;
 }
 
-// W = 16 step launches take the TMA form only when their gradient rows span
-// 16 GiB or more of addresses. Measured on GB300 (interleaved A/B, fraction of
-// the copy peak, LDG -> TMA form with two 88 KB stages): one FlatParameter of
-// 1e9 elements (rows 2 GB apart, 30 GiB span) 0.970 -> 1.004; 5e8 (15 GiB)
-// 1.001 -> 1.008; 3e8 (9 GiB) 1.006 -> 1.017; 2e8 (6 GiB) 1.011 -> 1.017; 1e8
-// (3 GiB) 1.008 -> 1.012; but the hybrid workload's Llama block at F = W = 16
-// (6.5 GiB) 1.041 -> 1.024. Span does not separate the last case from the 2e8
-// one, so the rule takes the form only where its gain is clear.
-constexpr uintptr_t kTma16Spread = uintptr_t(16) << 30;
+// W = 16 step launches take the TMA form when the gradient rows of some step
+// segment do not all lie a whole number of 2 KB apart: the LDG form's sixteen
+// simultaneous row streams then run below the copy peak, while the TMA form's
+// bulk copies do not care. Measured on GB300 (interleaved A/B, fraction of the
+// copy peak, LDG -> TMA form with two 88 KB stages; one FlatParameter of P
+// elements, so the rows are 2P bytes apart): rows a multiple of 512 B or 1 KB
+// apart (P = 1e8, 2e8, 3e8, 5e8, 1e9): 1.008 -> 1.012, 0.994 -> 1.012,
+// 1.006 -> 1.017, 1.001 -> 1.008, 0.972 -> 1.005; a multiple of 2, 4, 8, 16 or
+// 32 KB (P near 2e8, and the Llama block's 202,383,360): 1.042 -> 1.019,
+// 1.047 -> 1.022, 1.050 -> 1.024, 1.050 -> 1.027, 1.050 -> 1.027, 1.041 ->
+// 1.024; and near 1e9 with 2 KB and 16 KB: 1.025 -> 1.009, 1.040 -> 1.019.
+// The rows' span does not matter (3 to 30 GiB above).
+constexpr uintptr_t kTma16RowGrain = 2048;
+
+bool rows_off_grain(const Params& p) {
+  for (int k = 0; k < p.nseg; ++k) {
+    const Seg& d = p.seg[k];
+    if (d.kind != kStep) continue;
+    const uintptr_t base = reinterpret_cast<uintptr_t>(p.ptr[d.ptr]);
+    for (int r = 1; r < p.s.w; ++r)
+      if ((reinterpret_cast<uintptr_t>(p.ptr[d.ptr + r]) - base) % kTma16RowGrain != 0) return true;
+  }
+  return false;
+}
 
 // The TMA form pays off for launches that give every block enough chunks to
 // fill its pipeline and that hold either W = 8 steps whose positions each have
@@ -217,7 +232,7 @@ bool use_tma(const Params& p, int tma_grid) {
   if (step) {
     for (int k = 0; k < p.nseg; ++k)
       if (p.seg[k].kind == kZero) return false;
-    if (p.s.w == 16 && max_row_span(p) < kTma16Spread) return false;
+    if (p.s.w == 16 && !rows_off_grain(p)) return false;
   } else if (!copy) {
     return false;
   }

@@ -14,15 +14,15 @@
 // bulk copy per array and kInterleave = true (the host picks it when a
 // launch's gradient rows span 3 GiB or more of addresses) in four rounds of
 // quarter chunks over the arrays; for W = 16 (one copy per array, two stages
-// of 88 KB), the host picks it for launches whose gradient rows span 16 GiB or
-// more.
+// of 88 KB), the host picks it for launches whose gradient rows do not all lie
+// a multiple of 2 KB apart.
 //
 // Measured on GB300 against segment_kernel (same chunks, same arithmetic,
 // bit-identical results): W = 8 single-replica step launches gain 1-4 %
 // (Llama block 1.246 -> 1.206 ms); W <= 4, replica-heavy hybrid steps, short
 // launches and launches of reduce chunks lose, so the host uses this form only
 // for W = 8 launches made of one-replica step segments (and copies), for W = 16
-// ones whose rows span 16 GiB or more (see abi.cu), and for launches of copies
+// ones whose rows are not all 2 KB-aligned to each other (see abi.cu), and for launches of copies
 // only (and zero fills: pack, unpack, the gathers; 1-3.5 % faster), with at
 // least kTmaMinChunksPerBlock chunks per block.
 //

@@ -276,7 +276,7 @@ int fsdp_shard_step_grouped_launches(const fsdp_unit_args_t *units, int32_t n_un
  * receives how many of those launches use the TMA form of the kernel (bulk
  * copies into a shared-memory pipeline; chosen for W = 8 launches made of
  * one-replica step segments, and copies, for W = 16 ones whose gradient rows
- * span 16 GiB or more of addresses, and for launches of copies only, each with
+ * do not all lie a multiple of 2 KB apart, and for launches of copies only, each with
  * enough chunks to fill every SM's pipeline), *tma_interleaved_out (if not
  * NULL) how many of the W = 8 TMA launches stage their step chunks in four
  * interleaved rounds of quarter-chunk copies (chosen when a launch's gradient

@@ -237,6 +237,38 @@ def test_rank_range_and_grouped_parts_reject_bad_arguments():
     grouped([], HP, stream=0)
 
 
+def _plan_with_rows(W, F, stride_bytes, S, base=BASE):
+    """The plan of one all-ranks unit whose W gradient rows start stride_bytes apart (fake
+    device addresses: the plan reads no memory)."""
+    lay = fs.fsdp_flatten_layout([F * S], W, F)[0]
+    assert lay.shard_numel == S
+    padded = lay.padded_numel
+    assert stride_bytes >= 2 * padded
+    grads = [base + k * stride_bytes for k in range(W)]
+    top = base + W * stride_bytes + (1 << 30)
+    state = [top + i * S * 4 for i in range(3 * W)]
+    full = [top + 3 * W * S * 4 + g * padded * 2 for g in range(W // F)]
+    unit = dict(layout=lay, grads=grads, master=state[:W], exp_avg=state[W:2 * W], exp_avg_sq=state[2 * W:],
+                other_shards=None, full_out=full)
+    return fs.fsdp_shard_step_grouped_plan([unit], 0, W, interleaved=True)
+
+
+def test_w16_tma_form_follows_row_alignment():
+    """W = 16 single-replica launches large enough for the TMA form take it exactly when their
+    gradient rows do not all lie a multiple of 2 KB apart, whatever the rows' span; W = 8
+    launches take it either way, and replicated W = 16 launches never."""
+    S = 152 * 130 * 2048 // 16 + 8  # above 128 chunks per SM on a 152-SM GPU
+    row = 2 * 16 * S
+    grain = -(-row // 2048) * 2048
+    for stride, want in ((grain, (1, 0, 0)), (grain + 1024, (1, 1, 0)), (grain + 512, (1, 1, 0)),
+                         (grain + 4096, (1, 0, 0)), (grain + (30 << 30) // 15 // 2048 * 2048, (1, 0, 0)),
+                         (2_000_000_000, (1, 1, 0))):
+        assert _plan_with_rows(16, 16, stride, S) == want, stride
+    assert _plan_with_rows(8, 8, grain, 2 * S)[:2] == (1, 1)
+    assert _plan_with_rows(8, 8, grain + 1024, 2 * S)[:2] == (1, 1)
+    assert _plan_with_rows(16, 8, grain + 1024, S // 2 // 8 * 8) == (1, 0, 0)
+
+
 def test_pack_unpack_reject_bad_arguments():
     lay, offs = fs.fsdp_flatten_layout([10, 20, 30], 4)
     ts = [_addr(k) for k in range(3)]

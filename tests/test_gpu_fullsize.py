@@ -137,7 +137,7 @@ def test_sweep_1e9_every_element(ora, W):
     wl = bench.sweep_workload(n, W)
     units, info, keep = bench.build_all_ranks(wl, W, torch, fs, synth)
     # the TMA form at W = 8 (interleaved copies: rows 3 GiB or more apart) and at W = 16 (rows
-    # spanning 16 GiB or more), the LDG form at W = 2 and 4
+    # 2e9 bytes apart, not a multiple of 2 KB), the LDG form at W = 2 and 4
     tma, interleaved = (1 if W in (8, 16) else 0), (1 if W == 8 else 0)
     assert fs.fsdp_shard_step_grouped_plan(units, 0, W, interleaved=True) == (1, tma, interleaved)
     fs.fsdp_shard_step_grouped(units, 0, W, gu.adam_hyper(2))

@@ -1,15 +1,14 @@
 """The TMA form for W = 16 against the oracle, on every element.
 
 The library stages W = 16 single-replica steps through the TMA form (two
-88 KB stages) only when a launch's gradient rows span 16 GiB or more of
-addresses (the widest step segment of the launch decides). Here 16 rows are
-views into one buffer of about 17 GiB, the first and the last 17 GiB apart;
-only the rows themselves are written. Cases: every rank stepped with aligned
-and with ragged shards (the compared unit's own rows far apart), one rank
-stepped with the other shards gathered and special values (infinities, NaN,
-subnormals, signed zeros), each as a small unit beside a zero filler unit whose
-wide rows bring the launch to the form, and the plan's choice on both sides of
-the rule.
+88 KB stages) when the gradient rows of some step segment of the launch do not
+all lie a multiple of 2 KB apart. Here the 16 rows are views into one buffer,
+an odd multiple of 1 KB apart. Cases: every rank stepped with aligned and with
+ragged shards, one rank stepped with the other shards gathered and special
+values (infinities, NaN, subnormals, signed zeros), each as a small unit beside
+a zero filler unit whose rows bring the launch to the form, and the plan's
+choice on both sides of the rule (tests/test_abi_host.py checks the rule on
+the host alone, spans of many GiB included).
 """
 import numpy as np
 import pytest
@@ -22,7 +21,6 @@ pytestmark = pytest.mark.gpu
 fs = pytest.importorskip("fully_sharded_gb300")
 
 W = 16
-SPREAD = 17 << 30  # bytes between the first and the last row
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -34,44 +32,37 @@ def _cuda():
     torch.cuda.empty_cache()
 
 
-@pytest.fixture(scope="module")
-def wide():
-    """One int16 buffer large enough for 16 rows of up to 256 M elements spread over SPREAD bytes."""
+def _rows(n, on_grain=False):
+    """16 views of n bf16 elements in one buffer, 16-byte aligned, consecutive rows an odd
+    multiple of 1 KB apart (off the 2 KB grain), or a multiple of 2 KB apart."""
     torch = gu.torch()
-    buf = torch.empty(SPREAD // 2 + (1 << 28), dtype=torch.int16, device="cuda")
-    yield buf
-    del buf
-
-
-def _wide_views(buf, n):
-    """16 views of n elements, 16-byte aligned, the first and the last SPREAD bytes apart."""
-    step = (SPREAD // 2 // (W - 1)) // 8 * 8
-    assert n <= step and (W - 1) * step + n <= buf.numel()  # every row whole, none overlapping
-    views = [buf[k * step:k * step + n] for k in range(W)]
+    stride = -(-n // 1024) * 1024 + (0 if on_grain else 512)  # elements: 2 bytes each
+    buf = torch.empty(W * stride, dtype=torch.int16, device="cuda")
+    views = [buf[k * stride:k * stride + n] for k in range(W)]
     assert all(v.numel() == n for v in views)
-    assert views[-1].data_ptr() - views[0].data_ptr() >= 16 << 30
+    assert ((views[1].data_ptr() - views[0].data_ptr()) % 2048 == 0) == on_grain
     return views
 
 
-def _wide_rows(buf, grads):
-    """The host rows copied into wide views of `buf`."""
+def _rows_from(grads):
+    """The host rows copied into off-grain views."""
     torch = gu.torch()
-    rows = _wide_views(buf, grads[0].size)
+    rows = _rows(grads[0].size)
     for view, g in zip(rows, grads):
         view.copy_(torch.from_numpy(g.view(np.int16)))
     return rows
 
 
-def _wide_filler(buf, owned, local):
-    """A zero-filled unit with wide rows whose chunks bring the launch to the TMA form's
-    threshold (and, being the widest step segment, to its W = 16 instantiation)."""
+def _filler(owned, local):
+    """A zero-filled unit with off-grain rows whose chunks bring the launch to the TMA form's
+    threshold (and to its W = 16 instantiation)."""
     torch = gu.torch()
     sms = torch.cuda.get_device_properties(0).multi_processor_count
     need = 130 * sms
     # local rank: 4 step chunks and 15 gather chunks of 16 KB per 8192 shard elements
     S = 8192 * -(-need // (4 + W - 1)) if local else 2048 * -(-need // W)
     lay, _ = fs.fsdp_flatten_layout([W * S], W)
-    rows = _wide_views(buf, W * S)
+    rows = _rows(W * S)
     for r in rows:
         r.zero_()
     z = lambda n, dt: torch.zeros(n, dtype=dt, device="cuda")  # noqa: E731
@@ -99,7 +90,7 @@ def _inputs(seed, P):
 
 
 @pytest.mark.parametrize("align8", [False, True])
-def test_tma16_all_ranks_matches_oracle(ora, wide, align8):
+def test_tma16_all_ranks_matches_oracle(ora, align8):
     torch = gu.torch()
     S = _shard_len(align8)
     P = W * S
@@ -107,7 +98,7 @@ def test_tma16_all_ranks_matches_oracle(ora, wide, align8):
     assert lay.shard_numel == S
     grads, master, m, v = _inputs(160 + align8, P)
     sl = lambda a, r: a[r * S:(r + 1) * S]  # noqa: E731
-    units = [dict(layout=lay, grads=_wide_rows(wide, grads),
+    units = [dict(layout=lay, grads=_rows_from(grads),
                   master=[gu.to_dev(sl(master, r)) for r in range(W)],
                   exp_avg=[gu.to_dev(sl(m, r)) for r in range(W)],
                   exp_avg_sq=[gu.to_dev(sl(v, r)) for r in range(W)],
@@ -128,9 +119,9 @@ def test_tma16_all_ranks_matches_oracle(ora, wide, align8):
     gu.assert_same_bits(gu.to_host(u["full_out"][0]), ofull[0], "full")
 
 
-def test_tma16_local_rank_matches_oracle(ora, wide):
+def test_tma16_local_rank_matches_oracle(ora):
     """One rank stepped and the other 15 shards gathered (copy chunks through the same form),
-    a ragged unit beside the wide filler."""
+    a ragged unit beside the filler."""
     torch = gu.torch()
     rank = 11
     P = W * 300_001 - 5
@@ -147,7 +138,7 @@ def test_tma16_local_rank_matches_oracle(ora, wide):
                 exp_avg=[gu.to_dev(sl(m))], exp_avg_sq=[gu.to_dev(sl(v))],
                 other_shards=[None if k == rank else gu.to_dev(others[k]) for k in range(W)],
                 full_out=[torch.zeros(padded, dtype=torch.int16, device="cuda")])
-    units = [unit, _wide_filler(wide, [rank], True)]
+    units = [unit, _filler([rank], True)]
     assert fs.fsdp_shard_step_grouped_plan(units, rank, rank + 1, interleaved=True) == (1, 1, 0)
     fs.fsdp_shard_step_grouped(units, rank, rank + 1, gu.adam_hyper(9))
     torch.cuda.synchronize()
@@ -163,7 +154,7 @@ def test_tma16_local_rank_matches_oracle(ora, wide):
 
 
 @pytest.mark.parametrize("local", [False, True])
-def test_tma16_special_values(ora, wide, local):
+def test_tma16_special_values(ora, local):
     """Infinities, NaN, subnormal and signed-zero gradients and extreme masters through the
     W = 16 TMA form: every non-NaN output bit-identical, NaN exactly where the oracle has NaN."""
     torch = gu.torch()
@@ -183,7 +174,7 @@ def test_tma16_special_values(ora, wide, local):
                 exp_avg_sq=[gu.to_dev(sl(v, r)) for r in owned],
                 other_shards=[None if k in owned else gu.to_dev(others[k]) for k in range(W)] if local else None,
                 full_out=[torch.zeros(padded, dtype=torch.int16, device="cuda")])
-    units = [unit, _wide_filler(wide, owned, local)]
+    units = [unit, _filler(owned, local)]
     assert fs.fsdp_shard_step_grouped_plan(units, owned[0], owned[-1] + 1, interleaved=True) == (1, 1, 0)
     fs.fsdp_shard_step_grouped(units, owned[0], owned[-1] + 1, gu.adam_hyper(3))
     torch.cuda.synchronize()
@@ -211,16 +202,15 @@ def test_tma16_special_values(ora, wide, local):
     assert nan_seen > 0
 
 
-def test_tma16_rule_takes_only_wide_rows(wide):
-    """The same W = 16 unit runs on the LDG form when its rows sit close together, and on
-    the TMA form when they span 16 GiB or more (the plan, no launch)."""
+def test_tma16_rule_follows_row_alignment():
+    """The same W = 16 unit runs on the LDG form when its rows lie a multiple of 2 KB apart,
+    and on the TMA form when they do not (the plan, no launch)."""
     torch = gu.torch()
     S = _shard_len(True)
     P = W * S
     lay, _ = fs.fsdp_flatten_layout([P], W)
-    close = torch.empty((W, P), dtype=torch.int16, device="cuda")
     state = [torch.empty(S, device="cuda") for _ in range(3 * W)]
     unit = dict(layout=lay, master=state[:W], exp_avg=state[W:2 * W], exp_avg_sq=state[2 * W:],
                 other_shards=None, full_out=[torch.empty(P, dtype=torch.int16, device="cuda")])
-    assert fs.fsdp_shard_step_grouped_plan([dict(unit, grads=[close[k] for k in range(W)])], 0, W) == (1, 0)
-    assert fs.fsdp_shard_step_grouped_plan([dict(unit, grads=_wide_views(wide, P))], 0, W) == (1, 1)
+    assert fs.fsdp_shard_step_grouped_plan([dict(unit, grads=_rows(P, on_grain=True))], 0, W) == (1, 0)
+    assert fs.fsdp_shard_step_grouped_plan([dict(unit, grads=_rows(P))], 0, W) == (1, 1)
