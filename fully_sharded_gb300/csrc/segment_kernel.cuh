@@ -132,6 +132,13 @@ __device__ __forceinline__ void st_stream_f4(float* p, float4 v) {
 __device__ __forceinline__ void st_stream_u4(void* p, uint4 v) {
   __stcs(reinterpret_cast<uint4*>(p), v);
 }
+// 8 consecutive fp32 (one 32-byte sector) in one streaming store; p must be
+// 32-byte aligned.
+__device__ __forceinline__ void st_stream_f8(float* p, const float (&x)[8]) {
+  asm volatile("st.global.cs.v8.f32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(p), "f"(x[0]), "f"(x[1]), "f"(x[2]),
+               "f"(x[3]), "f"(x[4]), "f"(x[5]), "f"(x[6]), "f"(x[7])
+               : "memory");
+}
 
 // ------------------------------------------------------------- arithmetic
 

@@ -197,7 +197,14 @@ __device__ __forceinline__ uint32_t tma_chunk(const Params& p, const Seg& d, int
 // The consumers take 8 consecutive elements per thread (Map<false>): measured on
 // GB300, the split mapping of segment_kernel (two groups of 4, two 8-byte
 // shared-memory reads per row) made the Llama block's step 4.6 % slower here
-// (1.189 -> 1.244 ms; the 7B local-rank step 8.562 -> 8.580 ms).
+// (1.189 -> 1.244 ms; the 7B local-rank step 8.562 -> 8.580 ms). Each thread
+// stores its 8 new fp32 values of an array as one 32-byte sector when the
+// three state arrays are 32-byte aligned (else as two float4): a warp's store
+// then fills 32 whole sectors in one instruction instead of half of them in
+// each of two (interleaved A/B on GB300: Llama block 1.193 -> 1.183 ms, the
+// 1e8-element W = 8 step 0.596 -> 0.588 ms, the 1e9-element W = 16 step
+// 8.461 -> 8.344 ms, the 7B step unchanged at 8.56-8.57 ms). The LDG form
+// keeps its 16-byte accesses: there 32-byte loads and stores were 2-5 % slower.
 template <int W>
 __device__ __forceinline__ void tma_consume_step(const Params& p, const Seg& d, int64_t local,
                                                  const unsigned char* stage, int64_t nc) {
@@ -229,10 +236,22 @@ __device__ __forceinline__ void tma_consume_step(const Params& p, const Seg& d, 
     const int b = d.ptr + W;
 #pragma unroll
     for (int i = 0; i < 8; ++i) adam1(g[i], st.p[i], st.m[i], st.v[i], p.s);
-    store_state8<false>(st, static_cast<float*>(const_cast<void*>(p.ptr[b])),
-                        static_cast<float*>(const_cast<void*>(p.ptr[b + 1])),
-                        static_cast<float*>(const_cast<void*>(p.ptr[b + 2])),
-                        static_cast<uint16_t*>(const_cast<void*>(p.ptr[b + 3])), e0 + j);
+    float* mp = static_cast<float*>(const_cast<void*>(p.ptr[b]));
+    float* mm = static_cast<float*>(const_cast<void*>(p.ptr[b + 1]));
+    float* mv = static_cast<float*>(const_cast<void*>(p.ptr[b + 2]));
+    uint16_t* out = static_cast<uint16_t*>(const_cast<void*>(p.ptr[b + 3]));
+    const int64_t e = e0 + j;  // a multiple of 8 elements: 32 bytes of fp32
+    if (((reinterpret_cast<uintptr_t>(mp) | reinterpret_cast<uintptr_t>(mm) | reinterpret_cast<uintptr_t>(mv)) &
+         31u) == 0) {
+      st_stream_f8(mp + e, st.p);
+      st_stream_f8(mm + e, st.m);
+      st_stream_f8(mv + e, st.v);
+      if (out)
+        st_stream_u4(out + e, make_uint4(bf16x2_rn(st.p[0], st.p[1]), bf16x2_rn(st.p[2], st.p[3]),
+                                         bf16x2_rn(st.p[4], st.p[5]), bf16x2_rn(st.p[6], st.p[7])));
+    } else {
+      store_state8<false>(st, mp, mm, mv, out, e);
+    }
   } else {
     // this thread's elements beyond the staged part (the chunk's last < 8)
     int64_t end = d.n - e0;
