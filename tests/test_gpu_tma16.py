@@ -4,7 +4,8 @@ The library stages W = 16 single-replica steps through the TMA form (two
 88 KB stages) when the gradient rows of some step segment of the launch do not
 all lie a multiple of 2 KB apart. Here the 16 rows are views into one buffer,
 an odd multiple of 1 KB apart. Cases: every rank stepped with aligned and with
-ragged shards, one rank stepped with the other shards gathered and special
+ragged shards (and state views 16 bytes off 32-byte alignment, which the
+consumers store as two float4 instead of one 32-byte store), one rank stepped with the other shards gathered and special
 values (infinities, NaN, subnormals, signed zeros), each as a small unit beside
 a zero filler unit whose rows bring the launch to the form, and the plan's
 choice on both sides of the rule (tests/test_abi_host.py checks the rule on
@@ -15,6 +16,7 @@ import pytest
 
 import gpu_util as gu
 from test_gpu_special_values import _same_or_both_nan, _same_or_both_nan_bf16, _special_inputs
+from test_gpu_tma import _dev_at
 
 pytestmark = pytest.mark.gpu
 
@@ -89,8 +91,9 @@ def _inputs(seed, P):
     return grads, master, m, v
 
 
-@pytest.mark.parametrize("align8", [False, True])
-def test_tma16_all_ranks_matches_oracle(ora, align8):
+# state_off 4: the state views 16 bytes past 32-byte alignment (two float4 stores per array)
+@pytest.mark.parametrize("align8,state_off", [(False, 0), (True, 0), (True, 4)])
+def test_tma16_all_ranks_matches_oracle(ora, align8, state_off):
     torch = gu.torch()
     S = _shard_len(align8)
     P = W * S
@@ -99,10 +102,11 @@ def test_tma16_all_ranks_matches_oracle(ora, align8):
     grads, master, m, v = _inputs(160 + align8, P)
     sl = lambda a, r: a[r * S:(r + 1) * S]  # noqa: E731
     units = [dict(layout=lay, grads=_rows_from(grads),
-                  master=[gu.to_dev(sl(master, r)) for r in range(W)],
-                  exp_avg=[gu.to_dev(sl(m, r)) for r in range(W)],
-                  exp_avg_sq=[gu.to_dev(sl(v, r)) for r in range(W)],
+                  master=[_dev_at(sl(master, r), state_off) for r in range(W)],
+                  exp_avg=[_dev_at(sl(m, r), state_off) for r in range(W)],
+                  exp_avg_sq=[_dev_at(sl(v, r), state_off) for r in range(W)],
                   other_shards=None, full_out=[torch.zeros(P, dtype=torch.int16, device="cuda")])]
+    assert all(t.data_ptr() % 32 == 4 * state_off for t in units[0]["exp_avg_sq"])
     assert fs.fsdp_shard_step_grouped_plan(units, 0, W, interleaved=True) == (1, 1, 0)
     fs.fsdp_shard_step_grouped(units, 0, W, gu.adam_hyper(4))
     torch.cuda.synchronize()
