@@ -20,6 +20,17 @@ def to_dev(a: np.ndarray):
     return t.from_numpy(a.copy()).cuda()
 
 
+def to_dev_at(a: np.ndarray, off: int):
+    """A device copy of fp32 `a` that starts `off` elements into its own allocation
+    (off = 4: 16 bytes past the allocation's alignment)."""
+    if off == 0:
+        return to_dev(a)
+    t = torch()
+    buf = t.zeros(off + len(a), dtype=t.float32, device="cuda")
+    buf[off:] = to_dev(a)
+    return buf[off:]
+
+
 def to_host(x) -> np.ndarray:
     t = torch()
     a = x.detach().cpu()

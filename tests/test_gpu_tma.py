@@ -31,16 +31,6 @@ def _tma_shard_len(align8):
     return S - S % 8 + (0 if align8 else 3)
 
 
-def _dev_at(arr, off):
-    """A device copy of `arr` that starts `off` elements into its own allocation."""
-    torch = gu.torch()
-    if off == 0:
-        return gu.to_dev(arr)
-    t = torch.zeros(off + len(arr), dtype=torch.float32, device="cuda")
-    t[off:] = gu.to_dev(arr)
-    return t[off:]
-
-
 # (align8, state_off): S a multiple of 8 or not; the state views 32-byte aligned
 # (state_off 0: the consumers store a thread's 8 fp32 of an array as one 32-byte
 # sector) or 16 bytes past that (4: two float4 each)
@@ -59,9 +49,9 @@ def test_tma_form_matches_oracle(ora, align8, state_off):
     m = np.abs(rng.standard_normal(P, dtype=np.float32) * 1e-4)
     v = np.abs(rng.standard_normal(P, dtype=np.float32) * 1e-4)
     units = [dict(layout=lay, grads=[gu.to_dev(g) for g in grads],
-                  master=[_dev_at(master[r * S:(r + 1) * S], state_off) for r in range(W)],
-                  exp_avg=[_dev_at(m[r * S:(r + 1) * S], state_off) for r in range(W)],
-                  exp_avg_sq=[_dev_at(v[r * S:(r + 1) * S], state_off) for r in range(W)],
+                  master=[gu.to_dev_at(master[r * S:(r + 1) * S], state_off) for r in range(W)],
+                  exp_avg=[gu.to_dev_at(m[r * S:(r + 1) * S], state_off) for r in range(W)],
+                  exp_avg_sq=[gu.to_dev_at(v[r * S:(r + 1) * S], state_off) for r in range(W)],
                   other_shards=None, full_out=[torch.zeros(P, dtype=torch.int16, device="cuda")])]
     assert all(t.data_ptr() % 32 == 4 * state_off for t in units[0]["master"])
     assert fs.fsdp_shard_step_grouped_plan(units, 0, W) == (1, 1)

@@ -16,7 +16,6 @@ import pytest
 
 import gpu_util as gu
 from test_gpu_special_values import _same_or_both_nan, _same_or_both_nan_bf16, _special_inputs
-from test_gpu_tma import _dev_at
 
 pytestmark = pytest.mark.gpu
 
@@ -102,9 +101,9 @@ def test_tma16_all_ranks_matches_oracle(ora, align8, state_off):
     grads, master, m, v = _inputs(160 + align8, P)
     sl = lambda a, r: a[r * S:(r + 1) * S]  # noqa: E731
     units = [dict(layout=lay, grads=_rows_from(grads),
-                  master=[_dev_at(sl(master, r), state_off) for r in range(W)],
-                  exp_avg=[_dev_at(sl(m, r), state_off) for r in range(W)],
-                  exp_avg_sq=[_dev_at(sl(v, r), state_off) for r in range(W)],
+                  master=[gu.to_dev_at(sl(master, r), state_off) for r in range(W)],
+                  exp_avg=[gu.to_dev_at(sl(m, r), state_off) for r in range(W)],
+                  exp_avg_sq=[gu.to_dev_at(sl(v, r), state_off) for r in range(W)],
                   other_shards=None, full_out=[torch.zeros(P, dtype=torch.int16, device="cuda")])]
     assert all(t.data_ptr() % 32 == 4 * state_off for t in units[0]["exp_avg_sq"])
     assert fs.fsdp_shard_step_grouped_plan(units, 0, W, interleaved=True) == (1, 1, 0)
