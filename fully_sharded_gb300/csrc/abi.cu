@@ -194,7 +194,11 @@ bool has_step(const Params& p) {
 // 32 KB (P near 2e8, and the Llama block's 202,383,360): 1.042 -> 1.019,
 // 1.047 -> 1.022, 1.050 -> 1.024, 1.050 -> 1.027, 1.050 -> 1.027, 1.041 ->
 // 1.024; and near 1e9 with 2 KB and 16 KB: 1.025 -> 1.009, 1.040 -> 1.019.
-// The rows' span does not matter (3 to 30 GiB above).
+// The rows' span does not matter (3 to 30 GiB above). Since the TMA form's
+// consumers store state as 32-byte sectors it gained 1-2 % (the off-grain
+// launches above: 1.026-1.038), and the LDG form still leads on aligned rows:
+// 2 KB 1.042 -> 1.037, 4 KB 1.047 -> 1.038, 16 KB 1.051 -> 1.043 and
+// 1.054 -> 1.037.
 constexpr uintptr_t kTma16RowGrain = 2048;
 
 bool rows_off_grain(const Params& p) {

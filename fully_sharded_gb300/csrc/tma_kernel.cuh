@@ -18,8 +18,8 @@
 // a multiple of 2 KB apart.
 //
 // Measured on GB300 against segment_kernel (same chunks, same arithmetic,
-// bit-identical results): W = 8 single-replica step launches gain 1-4 %
-// (Llama block 1.246 -> 1.206 ms); W <= 4, replica-heavy hybrid steps, short
+// bit-identical results): W = 8 single-replica step launches gain 2-6 %
+// (Llama block 1.246 -> 1.179 ms); W <= 4, replica-heavy hybrid steps, short
 // launches and launches of reduce chunks lose, so the host uses this form only
 // for W = 8 launches made of one-replica step segments (and copies), for W = 16
 // ones whose rows are not all 2 KB-aligned to each other (see abi.cu), and for launches of copies
