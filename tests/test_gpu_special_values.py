@@ -203,3 +203,54 @@ def test_special_values_tma_form(ora, local):
         want = ofull[0]
     _same_or_both_nan_bf16(got, want, "full")
     assert nan_seen > 0
+
+
+# Hyper-parameters at the edges the library accepts: lr = 0 (the master keeps its value
+# except where the update is inf or NaN: 0 * inf), beta1 = beta2 = 0 (bias corrections of
+# exactly 1: m = g, v = g^2), eps = 0 (0 / 0 where v and g are both 0), beta2 one step
+# from 1 with t = 1 (a bias correction of about 1e-7), and a step count so large that
+# both bias corrections round to 1.
+HYPER_EDGES = [
+    (dict(lr=0.0, beta1=0.9, beta2=0.999, eps=1e-8), 3),
+    (dict(lr=1e-3, beta1=0.0, beta2=0.0, eps=1e-8), 1),
+    (dict(lr=1e-3, beta1=0.9, beta2=0.999, eps=0.0), 2),
+    (dict(lr=1e-2, beta1=0.5, beta2=0.9999999, eps=1e-12), 1),
+    (dict(lr=1e-3, beta1=0.9, beta2=0.999, eps=1e-8), 10 ** 9),
+]
+
+
+@pytest.mark.parametrize("W", [4, 2])
+@pytest.mark.parametrize("case", range(len(HYPER_EDGES)))
+def test_hyper_parameter_edges(ora, W, case):
+    """Every rank stepped, one small unit, on both element mappings of the LDG form (W = 4:
+    consecutive, W = 2: split); gradients with zeros and special values, v with zeros."""
+    torch = gu.torch()
+    hp, step = HYPER_EDGES[case]
+    P = W * 4096 - 1
+    lay, _ = fs.fsdp_flatten_layout([P], W)
+    S, padded = lay.shard_numel, lay.padded_numel
+    grads, master, m, v = _special_inputs(np.random.default_rng(500 + 7 * case + W), W, P, padded)
+    for g in grads:  # zero gradients beside the zero v's: 0 / 0 when eps = 0
+        g[: padded // 8] = 0
+    v[: padded // 16] = 0.0
+    sl = lambda a, r: a[r * S:(r + 1) * S].copy()  # noqa: E731
+    om, oe, ov = [sl(master, r) for r in range(W)], [sl(m, r) for r in range(W)], [sl(v, r) for r in range(W)]
+    ofull = [np.zeros(padded, np.uint16)]
+    ora.shard_step(grads, W, 0, W, om, oe, ov, None, ofull, step=step, **hp)
+    md = [gu.to_dev(sl(master, r)) for r in range(W)]
+    ed = [gu.to_dev(sl(m, r)) for r in range(W)]
+    vd = [gu.to_dev(sl(v, r)) for r in range(W)]
+    full = [torch.zeros(padded, dtype=torch.int16, device="cuda")]
+    fs.fsdp_shard_step([gu.to_dev(g) for g in grads], lay, 0, W, md, ed, vd, None, full,
+                       fs.AdamHyper(step=step, **hp))
+    torch.cuda.synchronize()
+    for r in range(W):
+        _same_or_both_nan(gu.to_host(md[r]), om[r], "master r%d" % r)
+        _same_or_both_nan(gu.to_host(ed[r]), oe[r], "exp_avg r%d" % r)
+        _same_or_both_nan(gu.to_host(vd[r]), ov[r], "exp_avg_sq r%d" % r)
+    _same_or_both_nan_bf16(gu.to_host(full[0]), ofull[0], "full")
+    if case == 0:  # lr = 0: every finite update leaves a nonzero master bit for bit as it was
+        before = np.concatenate([sl(master, r) for r in range(W)])
+        after = np.concatenate(om)
+        fin = np.isfinite(after) & np.isfinite(before) & (before != 0)
+        assert np.array_equal(after[fin].view(np.uint32), before[fin].view(np.uint32))
