@@ -506,7 +506,26 @@ int grouped(const fsdp_unit_args_t* units, int32_t n_units, int32_t rank_begin, 
     if (int rc = build_unit(units[i], rank_begin, rank_end, list, alias)) return rc;
   }
   if (!alias.ok()) return FSDP_EALIAS;
-  return launch(list, s, stream, count, tma_count, interleaved_count);
+  // Every unit's step segment first, then every gather: the launch then changes
+  // from step chunks to copy chunks once instead of once per unit, each change
+  // costing the pipeline about 2 us. Measured on GB300 (interleaved A/B, the
+  // local-rank step per unit -> steps first): the 7B step 8.567 -> 8.451 ms and
+  // 8.562 -> 8.471 ms (two boxes), four Llama blocks 1.031 -> 1.006 ms, GPT-2
+  // small 0.173 -> 0.165 ms; the gathers first instead were 2 % slower than this
+  // on the last two and equal on the 7B step.
+  SegmentList ordered;
+  for (int pass = 0; pass < 2; ++pass) {
+    for (size_t i = 0; i < list.seg.size(); ++i) {
+      const Seg& d = list.seg[i];
+      if ((pass == 0) != (d.kind == kStep)) continue;
+      Seg e = d;
+      e.ptr = static_cast<int32_t>(ordered.ptr.size());
+      ordered.seg.push_back(e);
+      const int np = list.pool_size(i);
+      for (int k = 0; k < np; ++k) ordered.ptr.push_back(list.ptr[d.ptr + k]);
+    }
+  }
+  return launch(ordered, s, stream, count, tma_count, interleaved_count);
 }
 
 }  // namespace

@@ -260,8 +260,11 @@ typedef struct {
 /* a7 over several units (e.g. one per transformer block, [math] "The sharding
  * unit": transformer_auto_wrap_policy makes each block a unit) in one launch
  * when they fit the launch's descriptor table, else in as few as needed.
- * All units share W, F, the owned rank range and the hyper-parameters. Units
- * must not share output memory. n_units == 0 is a no-op. */
+ * The launch runs every unit's fused step first and then every unit's gather
+ * of the other ranks' shards (the two touch disjoint memory, so the order
+ * does not change any result). All units share W, F, the owned rank range
+ * and the hyper-parameters. Units must not share output memory.
+ * n_units == 0 is a no-op. */
 int fsdp_shard_step_grouped(const fsdp_unit_args_t *units, int32_t n_units, int32_t rank_begin,
                             int32_t rank_end, const fsdp_adam_t *adam, fsdp_stream_t stream);
 
