@@ -4,7 +4,7 @@ Inputs are filled on the device by the seeded generator. Every workload of the
 benchmark's configurations is compared with the oracle on every element
 (tests/full_parity.py runs the oracle on all host cores): the Llama block and
 the GPT-2 units (TMA form), the Llama-7B local-rank headline (TMA form with
-interleaved copies; five units), the 1e9-element sweep at W = 2, 4, 8, 16 and
+interleaved copies; all 33 units), the 1e9-element sweep at W = 2, 4, 8, 16 and
 the hybrid workload at F = 16 and F = 4, whose every F also gives bit-identical
 state and parameters in every replica group (so F = 1 matches too). The two
 FlatParameters of more than 2^31 elements are checked on samples: the host
@@ -201,9 +201,10 @@ def test_flat_parameter_beyond_2_to_the_31_elements(ora, W, F, S):
 
 def test_llama7b_local_rank_every_element(ora):
     """The benchmark's headline workload and launch: one grouped launch over 33 units, rank 0,
-    on the TMA form with interleaved copies. For units 0, 1, 16, 31 and the root unit 32,
-    every element of the rank's master, exp_avg, exp_avg_sq, its own bf16 slice and the seven
-    gathered slices equals the oracle's shard_step."""
+    on the TMA form with interleaved copies (every unit's step, then every gather). For every
+    unit, the 32 blocks and the root unit, every element of the rank's master, exp_avg,
+    exp_avg_sq, its own bf16 slice and the seven gathered slices equals the oracle's
+    shard_step."""
     torch = gu.torch()
     wl = wls.LLAMA7B
     rank = 0
@@ -213,7 +214,7 @@ def test_llama7b_local_rank_every_element(ora):
     fs.fsdp_shard_step_grouped(units, rank, rank + 1, gu.adam_hyper(1))
     torch.cuda.synchronize()
     assert fs.fsdp_device_status() == 0
-    for u in (0, 1, 16, 31, 32):
+    for u in range(len(units)):
         lay = units[u]["layout"]
         S = lay.shard_numel
         regen = full_parity.state_regen(wl, u, lay.numel)(S, lay.shard_factor)
