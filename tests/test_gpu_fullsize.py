@@ -6,13 +6,9 @@ benchmark's configurations is compared with the oracle on every element
 the GPT-2 units (TMA form), the Llama-7B local-rank headline (TMA form with
 interleaved copies; all 33 units), the 1e9-element sweep at W = 2, 4, 8, 16 and
 the hybrid workload at F = 16 and F = 4, whose every F also gives bit-identical
-state and parameters in every replica group (so F = 1 matches too). The two
-FlatParameters of more than 2^31 elements are checked on samples: the host
-regenerates the inputs at sampled positions (around 2^30, 2^31 and the shard
-ends, and random ones), the oracle computes those outputs one by one, and they
-must equal the device outputs bit for bit.
+state and parameters in every replica group (so F = 1 matches too), and two
+FlatParameters of more than 2^31 elements.
 """
-import numpy as np
 import pytest
 
 import full_parity
@@ -33,59 +29,6 @@ def _cuda():
         pytest.skip("needs a CUDA GPU")
     yield
     torch.cuda.empty_cache()
-
-
-def sample_positions(n, offsets_in_shard=(), k=384, seed=0):
-    rng = np.random.default_rng(seed)
-    pts = set(range(min(n, 40))) | set(range(max(0, n - 40), n))
-    for b in (2047, 2048, 2049, 4095, 4096):
-        if b < n:
-            pts.add(b)
-    for o in offsets_in_shard:
-        for d in (-1, 0, 1):
-            if 0 <= o + d < n:
-                pts.add(o + d)
-    pts |= set(rng.integers(0, n, size=min(k, n)).tolist())
-    return np.array(sorted(pts), dtype=np.int64)
-
-
-def gather(t, idx):
-    torch = gu.torch()
-    return gu.to_host(t[torch.from_numpy(idx).cuda()])
-
-
-def oracle_at(ora, grad_rows, master, m, v, step):
-    """Oracle outputs for compact gathered inputs: fold over ranks, then Adam."""
-    g = ora.fold_mean(grad_rows)
-    p, mm, vv = master.copy(), m.copy(), v.copy()
-    bf = ora.adam(p, mm, vv, g, step=step, **gu.HP)
-    return p, mm, vv, bf
-
-
-def check_all_ranks_unit(ora, wl, u, unit, F, before, step, seed, extra_global=()):
-    """Sampled parity for one all-ranks unit; `before` holds host draws of the inputs.
-    `extra_global` adds positions (indices into the flat buffer) to every shard holding them."""
-    lay = unit["layout"]
-    W, S, P = lay.world_size, lay.shard_numel, lay.numel
-    R = W // F
-    for p in range(F):
-        j = sample_positions(S, [x - p * S for x in extra_global if 0 <= x - p * S < S], seed=seed + p)
-        i = p * S + j
-        rows = [synth.normal_bf16_at(wls.key_grad(wl, u, k, 0), i, wl.sigma_grad, n_valid=P) for k in range(W)]
-        master = synth.normal_f32_at(wls.key_master(wl, u), i, wl.sigma_master, n_valid=P)
-        if wl.sigma_state:
-            m = synth.normal_f32_at(wls.key_exp_avg(wl, u), i, wl.sigma_state, absval=True, n_valid=P)
-            v = synth.normal_f32_at(wls.key_exp_avg_sq(wl, u), i, wl.sigma_state, absval=True, n_valid=P)
-        else:
-            m = np.zeros(j.size, np.float32)
-            v = np.zeros(j.size, np.float32)
-        op, om, ov, obf = oracle_at(ora, rows, master, m, v, step)
-        for g in range(R):
-            r = g * F + p
-            gu.assert_same_bits(gather(unit["master"][r], j), op, "master u%d r%d" % (u, r))
-            gu.assert_same_bits(gather(unit["exp_avg"][r], j), om, "exp_avg u%d r%d" % (u, r))
-            gu.assert_same_bits(gather(unit["exp_avg_sq"][r], j), ov, "exp_avg_sq u%d r%d" % (u, r))
-            gu.assert_same_bits(gather(unit["full_out"][g], i), obf, "full u%d g%d" % (u, r))
 
 
 def every_element(ora, wl, units, rb, re, step, what, piece=1 << 20):
@@ -179,8 +122,8 @@ def test_flat_parameter_beyond_2_to_the_31_elements(ora, W, F, S):
     W = 2, F = 1 (the LDG form, two replicas): each shard is the whole padded buffer, so
     the kernel's element index itself passes 2^31. W = 8, F = 8 (the TMA form): the
     shards start beyond 2^31 elements of the gradient rows and the full buffer. Both
-    have a ragged last chunk (S mod 2048 != 0) and padding at the end; samples around
-    2^31, 2^30 and both ends of every shard are checked against the oracle."""
+    have a ragged last chunk (S mod 2048 != 0) and padding at the end; every element of
+    every replica is compared with the oracle."""
     torch = gu.torch()
     padded = F * S
     n = padded - (1 if W == 2 else 5)
@@ -193,8 +136,7 @@ def test_flat_parameter_beyond_2_to_the_31_elements(ora, W, F, S):
     assert (launches, tma) == (1, 1 if W == 8 else 0)
     fs.fsdp_shard_step_grouped(units, 0, W, gu.adam_hyper(1))
     torch.cuda.synchronize()
-    edges = [(1 << 31) + d for d in (-2, -1, 0, 1, 2)] + [n - 1, n, padded - 1, (1 << 30) - 1, 1 << 30]
-    check_all_ranks_unit(ora, wl, 0, units[0], F, None, 1, seed=40 + W, extra_global=edges)
+    every_element(ora, wl, units, 0, W, 1, "beyond 2^31, W=%d F=%d" % (W, F))
     del units, keep
     torch.cuda.empty_cache()
 
