@@ -240,7 +240,8 @@ bool use_tma(const Params& p, int tma_grid) {
   } else if (!copy) {
     return false;
   }
-  return p.total_chunks >= static_cast<int64_t>(kTmaMinChunksPerBlock) * tma_grid;
+  return p.total_chunks >=
+         static_cast<int64_t>(step ? kTmaMinStepChunksPerBlock : kTmaMinChunksPerBlock) * tma_grid;
 }
 
 // A TMA launch whose step segments have gradient rows spanning 3 GiB or more

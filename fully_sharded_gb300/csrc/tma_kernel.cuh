@@ -24,7 +24,11 @@
 // for W = 8 launches made of one-replica step segments (and copies), for W = 16
 // ones whose rows are not all 2 KB-aligned to each other (see abi.cu), and for launches of copies
 // only (and zero fills: pack, unpack, the gathers; 1-3.5 % faster), with at
-// least kTmaMinChunksPerBlock chunks per block.
+// least kTmaMinStepChunksPerBlock (steps) or kTmaMinChunksPerBlock (copies
+// only) chunks per block. Measured on GB300 (interleaved A/B, LDG -> TMA form):
+// W = 8 steps of 64-96 chunks per block 1.4-3.2 % faster and W = 16 ones
+// 0.5-1.5 %, 32 chunks per block 1-1.5 % slower; copies alone of 64 chunks per
+// block 3.5 % slower, of 128 and more faster.
 //
 // Every mbarrier wait is bounded in time (Params::wait_limit_ns, read from
 // %globaltimer): when a wait runs out the block sets bit 0 of g_fsdp_status,
@@ -43,7 +47,8 @@ namespace fsdp {
 constexpr int kTmaConsumerWarps = 8;
 constexpr int kTmaThreads = (kTmaConsumerWarps + 1) * 32;
 constexpr int kTmaStages = 4;  // 4 x 56 KB at W = 8 (W = 16: 2 x 88 KB)
-constexpr int kTmaMinChunksPerBlock = 128;
+constexpr int kTmaMinChunksPerBlock = 128;     // launches of copies only
+constexpr int kTmaMinStepChunksPerBlock = 64;  // launches with step chunks
 constexpr uint64_t kDefaultWaitLimitNs = 2000000000ull;  // 2 s
 
 template <int W>
