@@ -95,8 +95,10 @@ int grid_capacity(int variant, int* err) {
     if (tma && (cudaFuncSetAttribute(kernel_of(variant), cudaFuncAttributeMaxDynamicSharedMemorySize, smem) !=
                     cudaSuccess ||
                 (variant == kTmaVariant &&
-                 cudaFuncSetAttribute(reinterpret_cast<const void*>(&tma_kernel<8, true>),
-                                      cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess))) {
+                 (cudaFuncSetAttribute(reinterpret_cast<const void*>(&tma_kernel<8, true>),
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess ||
+                  cudaFuncSetAttribute(reinterpret_cast<const void*>(&tma_kernel<8, true, true>),
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)))) {
       *err = FSDP_ECUDA;
       return 0;
     }
@@ -139,7 +141,7 @@ cudaError_t launch_variant(const Params& p, int grid, cudaStream_t stream) {
   return e != cudaSuccess ? e : cudaGetLastError();
 }
 
-template <int W, bool kInterleave>
+template <int W, bool kInterleave, bool kOutOfLine = false>
 cudaError_t launch_tma_form(const Params& p, int grid, cudaStream_t stream) {
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3(grid);
@@ -151,12 +153,16 @@ cudaError_t launch_tma_form(const Params& p, int grid, cudaStream_t stream) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  const cudaError_t e = cudaLaunchKernelEx(&cfg, tma_kernel<W, kInterleave>, p);
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, tma_kernel<W, kInterleave, kOutOfLine>, p);
   return e != cudaSuccess ? e : cudaGetLastError();
 }
 
-// The W = 8 instantiations (copy-only launches take them whatever the W of the call).
-cudaError_t launch_tma(const Params& p, int grid, cudaStream_t stream, bool interleave = false) {
+// The W = 8 instantiations (copy-only launches take them whatever the W of the call);
+// interleaved launches holding copy chunks take the one with its unstaged paths out
+// of line (see tma_unstaged).
+cudaError_t launch_tma(const Params& p, int grid, cudaStream_t stream, bool interleave = false,
+                       bool copies = false) {
+  if (interleave && copies) return launch_tma_form<8, true, true>(p, grid, stream);
   return interleave ? launch_tma_form<8, true>(p, grid, stream) : launch_tma_form<8, false>(p, grid, stream);
 }
 
@@ -346,9 +352,10 @@ int launch(const SegmentList& list, const Scalars& s, cudaStream_t stream, int* 
       continue;
     }
     if (tma) {
-      if (launch_tma(p, static_cast<int>(std::min<int64_t>(chunks, tma_cap)), stream, wants_interleave(p)) !=
-          cudaSuccess)
-        return FSDP_ECUDA;
+      bool copies = false;
+      for (int k = 0; k < p.nseg; ++k) copies = copies || p.seg[k].kind == kCopy;
+      const int grid = static_cast<int>(std::min<int64_t>(chunks, tma_cap));
+      if (launch_tma(p, grid, stream, wants_interleave(p), copies) != cudaSuccess) return FSDP_ECUDA;
       continue;
     }
     const bool split = wants_split(p);

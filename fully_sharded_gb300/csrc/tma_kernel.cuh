@@ -285,12 +285,15 @@ __device__ __forceinline__ void tma_store_copy(const Params& p, const Seg& d, in
 }
 
 // The chunks the producer did not stage, run from global memory as in
-// segment_kernel. The interleaved instantiation calls this out of line, so that
+// segment_kernel. With kOutOfLine the kernel calls this out of line, so that
 // its staged paths are compiled without the fallbacks (108 registers instead of
-// 128); measured on GB300 (interleaved A/B, two boxes): the 7B local-rank step
-// 8.467 -> 8.402 and 8.470 -> 8.410 ms, the all-ranks 1e9 / 5e8-element W = 8
-// steps 0.1-0.4 % slower; in the one-copy instantiation it cost the Llama
-// block 1.6 %, which therefore keeps the fallbacks inline.
+// 128). Measured on GB300 (interleaved A/B): the interleaved launches that hold
+// copy chunks (the 7B local-rank step and its gathers) gain, 8.467 -> 8.402,
+// 8.470 -> 8.410 and 8.448 -> 8.404 ms on three boxes; the interleaved
+// all-ranks steps (no copies) lose 0.1-1.6 % (1e9 elements: 5.972 -> 6.066 ms),
+// and so do the one-copy launches (the Llama block 1.6 %, four Llama blocks in
+// the local-rank mode 0.4 %). So only interleaved launches with copy chunks
+// take it.
 template <int W>
 __device__ __noinline__ void tma_unstaged(const Params& p, const Seg& d, int64_t l) {
   switch (d.kind) {
@@ -302,7 +305,7 @@ __device__ __noinline__ void tma_unstaged(const Params& p, const Seg& d, int64_t
   }
 }
 
-template <int W, bool kInterleave>
+template <int W, bool kInterleave, bool kOutOfLine = false>
 __global__ void __launch_bounds__(kTmaThreads, 1) tma_kernel(const __grid_constant__ Params p) {
   extern __shared__ __align__(128) unsigned char smem[];
   __shared__ __align__(8) uint64_t full_bar[TmaCfg<W>::kStages];
@@ -368,7 +371,7 @@ __global__ void __launch_bounds__(kTmaThreads, 1) tma_kernel(const __grid_consta
       tma_consume_step<W>(p, d, l, st, staged);
     } else if (bytes != 0) {
       tma_store_copy(p, d, l, st, staged);
-    } else if constexpr (kInterleave) {
+    } else if constexpr (kOutOfLine) {
       tma_unstaged<W>(p, d, l);
     } else {
       switch (d.kind) {
