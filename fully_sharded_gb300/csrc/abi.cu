@@ -33,11 +33,13 @@ constexpr int kMaxDevices = 64;
 // Kernel variants: 0..5 the LDG form for W = 1, 2, 4, 8, 16 and any W with the
 // 8-consecutive-element mapping, 6 the TMA form (W = 8), 7..12 the LDG form
 // again with the split mapping (Map<true> in segment_kernel.cuh), 13 the TMA
-// form for W = 16.
+// form for W = 16, 14..19 the LDG form with the realigned path (launches that
+// hold step segments off 16-byte alignment: kPhased).
 constexpr int kTmaVariant = 6;
 constexpr int kSplitVariants = 7;
 constexpr int kTma16Variant = 13;
-constexpr int kNumVariants = 14;
+constexpr int kRealignVariants = 14;  // 14..19: the LDG form with the realigned path
+constexpr int kNumVariants = 20;
 
 std::atomic<int> g_sm_count[kMaxDevices];
 std::atomic<int> g_blocks_per_sm[kMaxDevices][kNumVariants];
@@ -53,21 +55,22 @@ int variant_of(int w) {
   }
 }
 
-template <bool kSplit>
+template <bool kSplit, bool kWithRealign = false>
 const void* ldg_kernel_of(int variant) {
   switch (variant) {
-    case 0: return reinterpret_cast<const void*>(&segment_kernel<1, kSplit>);
-    case 1: return reinterpret_cast<const void*>(&segment_kernel<2, kSplit>);
-    case 2: return reinterpret_cast<const void*>(&segment_kernel<4, kSplit>);
-    case 3: return reinterpret_cast<const void*>(&segment_kernel<8, kSplit>);
-    case 4: return reinterpret_cast<const void*>(&segment_kernel<16, kSplit>);
-    default: return reinterpret_cast<const void*>(&segment_kernel<0, kSplit>);
+    case 0: return reinterpret_cast<const void*>(&segment_kernel<1, kSplit, kWithRealign>);
+    case 1: return reinterpret_cast<const void*>(&segment_kernel<2, kSplit, kWithRealign>);
+    case 2: return reinterpret_cast<const void*>(&segment_kernel<4, kSplit, kWithRealign>);
+    case 3: return reinterpret_cast<const void*>(&segment_kernel<8, kSplit, kWithRealign>);
+    case 4: return reinterpret_cast<const void*>(&segment_kernel<16, kSplit, kWithRealign>);
+    default: return reinterpret_cast<const void*>(&segment_kernel<0, kSplit, kWithRealign>);
   }
 }
 
 const void* kernel_of(int variant) {
   if (variant == kTmaVariant) return reinterpret_cast<const void*>(&tma_kernel<8, false>);
   if (variant == kTma16Variant) return reinterpret_cast<const void*>(&tma_kernel<16, false>);
+  if (variant >= kRealignVariants) return ldg_kernel_of<false, true>(variant - kRealignVariants);
   return variant >= kSplitVariants ? ldg_kernel_of<true>(variant - kSplitVariants) : ldg_kernel_of<false>(variant);
 }
 
@@ -108,7 +111,9 @@ int grid_capacity(int variant, int* err) {
       *err = FSDP_ECUDA;
       return 0;
     }
-    const int w_variant = variant >= kSplitVariants ? variant - kSplitVariants : variant;
+    const int w_variant = variant >= kRealignVariants ? variant - kRealignVariants
+                          : variant >= kSplitVariants ? variant - kSplitVariants
+                                                      : variant;
     if (!tma && w_variant < 5 && per_sm > kBlocksPerSm) per_sm = kBlocksPerSm;  // fixed-W LDG variants
     g_blocks_per_sm[dev][variant].store(per_sm, std::memory_order_relaxed);
   }
@@ -125,7 +130,7 @@ int64_t chunks_of(const Seg& d) {
 // 1e7-element step 66.3 -> 64.5 us, 7B local-rank step 8.64 -> 8.57 ms); the
 // kernel's griddepcontrol.wait keeps every memory access after the previous
 // kernel has completed.
-template <int W, bool kSplit>
+template <int W, bool kSplit, bool kWithRealign = false>
 cudaError_t launch_variant(const Params& p, int grid, cudaStream_t stream) {
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3(grid);
@@ -137,7 +142,7 @@ cudaError_t launch_variant(const Params& p, int grid, cudaStream_t stream) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  const cudaError_t e = cudaLaunchKernelEx(&cfg, segment_kernel<W, kSplit>, p);
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, segment_kernel<W, kSplit, kWithRealign>, p);
   return e != cudaSuccess ? e : cudaGetLastError();
 }
 
@@ -228,10 +233,14 @@ bool rows_off_grain(const Params& p) {
 // 24 warps per SM carry such chunks better than the TMA form's 8 consumers.
 bool use_tma(const Params& p, int tma_grid) {
   bool step = false, copy = false;
+  int64_t step_chunks = 0, phased_chunks = 0;
   for (int k = 0; k < p.nseg; ++k) {
     const Seg& d = p.seg[k];
     if (d.kind == kStep) {
       if (d.nrep != 1 || (p.s.w != 8 && p.s.w != 16)) return false;
+      const int64_t c = (d.n + kChunkElems - 1) / kChunkElems;
+      step_chunks += c;
+      if (d.width == kPhased) phased_chunks += c;
       step = true;
     } else if (d.kind == kCopy) {
       copy = true;
@@ -243,6 +252,10 @@ bool use_tma(const Params& p, int tma_grid) {
     for (int k = 0; k < p.nseg; ++k)
       if (p.seg[k].kind == kZero) return false;
     if (p.s.w == 16 && !rows_off_grain(p)) return false;
+    // the TMA form runs segments with rows or state off alignment by a phase on
+    // the scalar path (the realigned one would raise its registers): launches
+    // made mostly of them go to the LDG form
+    if (phased_chunks * 8 > step_chunks) return false;
   } else if (!copy) {
     return false;
   }
@@ -277,6 +290,7 @@ bool wants_split(const Params& p) {
       any = true;
     } else if (d.kind == kStep) {
       if (2 * d.nrep < p.s.w) return false;
+      if (d.width == kPhased) return false;  // the realigned path has the consecutive mapping
       any = true;
     } else if (d.kind == kReduce) {
       return false;
@@ -356,6 +370,24 @@ int launch(const SegmentList& list, const Scalars& s, cudaStream_t stream, int* 
       for (int k = 0; k < p.nseg; ++k) copies = copies || p.seg[k].kind == kCopy;
       const int grid = static_cast<int>(std::min<int64_t>(chunks, tma_cap));
       if (launch_tma(p, grid, stream, wants_interleave(p), copies) != cudaSuccess) return FSDP_ECUDA;
+      continue;
+    }
+    bool realign = false;
+    for (int k = 0; k < p.nseg; ++k) realign = realign || (p.seg[k].kind == kStep && p.seg[k].width == kPhased);
+    if (realign) {
+      const int cap = grid_capacity(variant + kRealignVariants, &err);
+      if (err != FSDP_OK) return err;
+      const int grid = static_cast<int>(std::min<int64_t>(chunks, cap));
+      cudaError_t e;
+      switch (variant) {
+        case 0: e = launch_variant<1, false, true>(p, grid, stream); break;
+        case 1: e = launch_variant<2, false, true>(p, grid, stream); break;
+        case 2: e = launch_variant<4, false, true>(p, grid, stream); break;
+        case 3: e = launch_variant<8, false, true>(p, grid, stream); break;
+        case 4: e = launch_variant<16, false, true>(p, grid, stream); break;
+        default: e = launch_variant<0, false, true>(p, grid, stream); break;
+      }
+      if (e != cudaSuccess) return FSDP_ECUDA;
       continue;
     }
     const bool split = wants_split(p);

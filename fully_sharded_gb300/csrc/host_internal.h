@@ -23,6 +23,9 @@ struct SegmentList {
   static bool aligned16(const void* q) { return (reinterpret_cast<uintptr_t>(q) & 15u) == 0; }
 
   // kStep / kReduce / kAdam: `ptrs` in pool order; width 16 iff all are aligned.
+  // A kStep segment with some pointer off 16-byte alignment but every pointer
+  // aligned to its element (2 bytes for rows and outputs, 4 for state) gets
+  // kPhased (the realigned vector path).
   void add_elementwise(SegKind kind, int64_t n, int nrep, const std::vector<const void*>& ptrs) {
     if (n <= 0) return;
     bool ok = true;
@@ -33,8 +36,26 @@ struct SegmentList {
     d.nrep = nrep;
     d.ptr = static_cast<int32_t>(ptr.size());
     d.width = ok ? 16 : 0;
+    if (!ok && kind == kStep) d.width = step_phases(nrep, ptrs);
     seg.push_back(d);
     ptr.insert(ptr.end(), ptrs.begin(), ptrs.end());
+  }
+
+  // The width code of a step segment (not every pointer 16-byte aligned) whose
+  // pointers are all aligned to their elements: kPhased, else 0.
+  static int step_phases(int nrep, const std::vector<const void*>& ptrs) {
+    const size_t w = ptrs.size() - 4 * static_cast<size_t>(nrep);
+    if (nrep < 1 || w < 1 || w > ptrs.size()) return 0;
+    const auto low = [](const void* q) { return reinterpret_cast<uintptr_t>(q) & 15u; };
+    for (size_t k = 0; k < w; ++k)
+      if (!ptrs[k] || (low(ptrs[k]) & 1u)) return 0;
+    for (int r = 0; r < nrep; ++r) {
+      const size_t b = w + 4 * static_cast<size_t>(r);
+      for (int a = 0; a < 3; ++a)
+        if (!ptrs[b + a] || (low(ptrs[b + a]) & 3u)) return 0;
+      if (!ptrs[b + 3] || (low(ptrs[b + 3]) & 1u)) return 0;
+    }
+    return kPhased;
   }
 
   void add_bytes(SegKind kind, const void* src, void* dst, int64_t bytes) {

@@ -69,6 +69,11 @@ constexpr int kBlocksPerSm = 3;
 
 enum SegKind : int32_t { kStep = 0, kReduce = 1, kAdam = 2, kCopy = 3, kZero = 4 };
 
+// Width code of a step segment with some pointer off 16-byte alignment but every
+// pointer aligned to its element (2 bytes for rows and outputs, 4 for state):
+// its chunks take the realigned vector path.
+constexpr int32_t kPhased = 32;
+
 // One segment. Pointer pool layout (Params::ptr, starting at `ptr`):
 //   kStep   : W gradient rows (bf16, already offset to the position),
 //             then nrep x {master, exp_avg, exp_avg_sq, bf16 out}
@@ -83,6 +88,7 @@ struct Seg {
   int32_t nrep;       // kStep: replicas updated from the reduced gradient
   int32_t ptr;        // first pool entry
   int32_t width;      // kStep/kReduce/kAdam: 16 if every pointer is 16-byte aligned, else 0;
+                      // kStep also kPhased (see there);
                       // kCopy/kZero: access width in bytes (16, 8, 4, 2 or 1)
 };
 
@@ -226,6 +232,67 @@ __device__ __forceinline__ void add_row(float (&acc)[8], const RowLoad<kSplit>& 
   }
 }
 
+// The 8 bf16 values that start `phase` bytes (2..14, even) past the 16-byte
+// boundary `al`, from the two aligned 16-byte blocks at al and al + 16: a shift
+// by whole words (phase / 4, by selects on its two bits: the phase is the same
+// for every thread of a row) and then by half a word. The 32 bytes read stay within the pages
+// of the 16 bytes used (page boundaries are 16-byte aligned).
+__device__ __forceinline__ uint4 load_row_realigned(const unsigned char* al, int phase) {
+  const uint4 lo = ld_stream_u4(al), hi = ld_stream_u4(al + 16);
+  uint32_t w[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
+  const bool by2 = (phase & 8) != 0, by1 = (phase & 4) != 0;
+#pragma unroll
+  for (int i = 0; i < 6; ++i) w[i] = by2 ? w[i + 2] : w[i];
+#pragma unroll
+  for (int i = 0; i < 5; ++i) w[i] = by1 ? w[i + 1] : w[i];
+  const uint32_t h = (phase & 2) ? 16u : 0u;
+  return make_uint4(__funnelshift_r(w[0], w[1], h), __funnelshift_r(w[1], w[2], h), __funnelshift_r(w[2], w[3], h),
+                    __funnelshift_r(w[3], w[4], h));
+}
+
+// 8 fp32 values that start `phase` bytes (4, 8 or 12) past the 16-byte boundary
+// `al`, from the three aligned 16-byte blocks from al on (the same shifts by
+// whole words as load_row_realigned; the reads stay within the pages of the
+// 32 bytes used).
+__device__ __forceinline__ void load_f32x8_realigned(const float* al, int phase, float (&x)[8]) {
+  const float4 a = ld_stream_f4(al), b = ld_stream_f4(al + 4), c = ld_stream_f4(al + 8);
+  float w[12] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w, c.x, c.y, c.z, c.w};
+  const bool by2 = (phase & 8) != 0, by1 = (phase & 4) != 0;
+#pragma unroll
+  for (int i = 0; i < 10; ++i) w[i] = by2 ? w[i + 2] : w[i];
+#pragma unroll
+  for (int i = 0; i < 9; ++i) w[i] = by1 ? w[i + 1] : w[i];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) x[i] = w[i];
+}
+
+// fold8 (consecutive mapping) for rows at any even byte phase: each row's
+// phase is read from its pointer (the same for every thread: e is a multiple of
+// 8 elements, 16 bytes); the thread's 8 elements start at e.
+template <int W>
+__device__ __forceinline__ void fold8_realigned(const Params& p, const Seg& d, int64_t e, float (&g)[8]) {
+#pragma unroll
+  for (int i = 0; i < 8; ++i) g[i] = 0.0f;
+  const int w = W > 0 ? W : p.s.w;
+  constexpr int kBatch = (W > 0 && W < 8) ? W : 8;
+  for (int k0 = 0; k0 < w; k0 += kBatch) {
+    uint4 r[kBatch];
+#pragma unroll
+    for (int k = 0; k < kBatch; ++k)
+      if (W > 0 || k0 + k < w) {
+        const uint16_t* row = static_cast<const uint16_t*>(p.ptr[d.ptr + k0 + k]) + e;
+        const int phase = static_cast<int>(reinterpret_cast<uintptr_t>(row) & 15u);
+        r[k] = phase == 0 ? ld_stream_u4(row)
+                          : load_row_realigned(reinterpret_cast<const unsigned char*>(row) - phase, phase);
+      }
+#pragma unroll
+    for (int k = 0; k < kBatch; ++k)
+      if (W > 0 || k0 + k < w) add_bf16x8(g, r[k]);
+  }
+#pragma unroll
+  for (int i = 0; i < 8; ++i) g[i] = mean_of<W>(g[i], p.s);
+}
+
 // Reduced gradient of a thread's 8 elements (first group at e): the rows of a
 // batch (up to 8) are all loaded first (independent loads in flight), then
 // folded in rank order.
@@ -348,7 +415,93 @@ __device__ __forceinline__ void step_scalar(const Params& p, const Seg& d, int64
   }
 }
 
-template <int W, bool kSplit>
+// The state of a thread's 8 elements from arrays at any 4-byte phase (each
+// array's own, read from its pointer).
+__device__ __forceinline__ void load_f32x8_any(const float* q, float (&x)[8]) {
+  const int phase = static_cast<int>(reinterpret_cast<uintptr_t>(q) & 15u);
+  if (phase == 0) {
+    const float4 a = ld_stream_f4(q), b = ld_stream_f4(q + 4);
+    x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
+    x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
+  } else {
+    load_f32x8_realigned(q - phase / 4, phase, x);
+  }
+}
+
+// A warp's 256 results of one array, thread `lane` holding elements 8 lane ..
+// 8 lane + 7, stored through the warp's staging row `buf` so that every store
+// instruction writes 32 consecutive elements (q: the warp's first element).
+__device__ __forceinline__ void store_f32_transposed(float* buf, float* q, const float (&x)[8], int lane) {
+  reinterpret_cast<float4*>(buf)[2 * lane] = make_float4(x[0], x[1], x[2], x[3]);
+  reinterpret_cast<float4*>(buf)[2 * lane + 1] = make_float4(x[4], x[5], x[6], x[7]);
+  __syncwarp();
+#pragma unroll
+  for (int j = 0; j < 8; ++j) __stcs(q + 32 * j + lane, buf[32 * j + lane]);
+  __syncwarp();
+}
+__device__ __forceinline__ void store_bf16_transposed(float* buf, uint16_t* q, const float (&x)[8], int lane) {
+  reinterpret_cast<uint4*>(buf)[lane] = make_uint4(bf16x2_rn(x[0], x[1]), bf16x2_rn(x[2], x[3]),
+                                                   bf16x2_rn(x[4], x[5]), bf16x2_rn(x[6], x[7]));
+  __syncwarp();
+  const unsigned short* b16 = reinterpret_cast<const unsigned short*>(buf);
+#pragma unroll
+  for (int j = 0; j < 8; ++j) __stcs(reinterpret_cast<unsigned short*>(q) + 32 * j + lane, b16[32 * j + lane]);
+  __syncwarp();
+}
+
+// A step chunk of a kPhased segment (consecutive mapping). Each warp covers 256
+// consecutive elements: rows read as aligned 16-byte blocks shifted into place,
+// state read as aligned blocks shifted by whole words (every pointer at its own
+// phase), results stored through a per-warp staging row in shared memory so
+// that each store instruction writes 32 consecutive elements. A warp whose 256
+// elements pass the segment's end takes one element per lane. Same arithmetic
+// in the same order as the aligned path. Out of line, so that the aligned path
+// keeps its registers.
+template <int W>
+__device__ __noinline__ void step_chunk_realigned(const Params& p, const Seg& d, int64_t e0) {
+  __shared__ __align__(16) float stage[kThreads / 32][32 * kVec];
+  const int w = W > 0 ? W : p.s.w;
+  const int warp = static_cast<int>(threadIdx.x / 32), lane = static_cast<int>(threadIdx.x % 32);
+  const int64_t ew = e0 + int64_t(warp) * 32 * kVec;  // the warp's first element
+  if (ew >= d.n) return;
+  if (ew + 32 * kVec > d.n) {
+    for (int64_t i = ew + lane; i < d.n; i += 32) step_scalar<W>(p, d, i);
+    return;
+  }
+  const int64_t e = ew + int64_t(lane) * kVec;
+  const int b0 = d.ptr + w;
+  State8 st;
+  load_f32x8_any(static_cast<const float*>(p.ptr[b0]) + e, st.p);
+  load_f32x8_any(static_cast<const float*>(p.ptr[b0 + 1]) + e, st.m);
+  load_f32x8_any(static_cast<const float*>(p.ptr[b0 + 2]) + e, st.v);
+  float g[8];
+  fold8_realigned<W>(p, d, e, g);
+  float* buf = stage[warp];
+  for (int r = 0; r < d.nrep; ++r) {
+    const int b = b0 + 4 * r;
+    float* mp = static_cast<float*>(const_cast<void*>(p.ptr[b]));
+    float* mm = static_cast<float*>(const_cast<void*>(p.ptr[b + 1]));
+    float* mv = static_cast<float*>(const_cast<void*>(p.ptr[b + 2]));
+    uint16_t* out = static_cast<uint16_t*>(const_cast<void*>(p.ptr[b + 3]));
+    if (r > 0) {
+      load_f32x8_any(mp + e, st.p);
+      load_f32x8_any(mm + e, st.m);
+      load_f32x8_any(mv + e, st.v);
+    }
+#pragma unroll
+    for (int i = 0; i < 8; ++i) adam1(g[i], st.p[i], st.m[i], st.v[i], p.s);
+    store_f32_transposed(buf, mp + ew, st.p, lane);
+    store_f32_transposed(buf, mm + ew, st.m, lane);
+    store_f32_transposed(buf, mv + ew, st.v, lane);
+    store_bf16_transposed(buf, out + ew, st.p, lane);
+  }
+}
+
+// kRealign: kPhased segments take the realigned path, else the scalar one. Only
+// the kernel instantiations for launches that hold kPhased segments include it:
+// reachable, its code and its shared-memory staging rows slowed the aligned
+// path by 2-5 % (registers, spills, shared memory).
+template <int W, bool kSplit, bool kRealign = false>
 __device__ __forceinline__ void step_chunk(const Params& p, const Seg& d, int64_t e0) {
   const int w = W > 0 ? W : p.s.w;
   if (d.width == 16) {
@@ -382,6 +535,12 @@ __device__ __forceinline__ void step_chunk(const Params& p, const Seg& d, int64_
       }
     }
   } else {
+    if constexpr (!kSplit && kRealign) {
+      if (d.width == kPhased) {  // pointers off 16-byte alignment, each at its own phase
+        step_chunk_realigned<W>(p, d, e0);
+        return;
+      }
+    }
 #pragma unroll 1
     for (int k = 0; k < kVec; ++k) {
       const int64_t i = e0 + int64_t(k) * kThreads + threadIdx.x;
@@ -504,7 +663,9 @@ __device__ __forceinline__ void bytes_chunk(const Params& p, const Seg& d, int64
 
 // -------------------------------------------------------------- the kernel
 
-template <int W, bool kSplit>
+// kWithRealign: the instantiation for launches that hold kPhased step segments
+// (the consecutive mapping, with the realigned path).
+template <int W, bool kSplit, bool kWithRealign = false>
 __global__ void __launch_bounds__(kThreads, (W > 0 ? kBlocksPerSm : 2))
     segment_kernel(const __grid_constant__ Params p) {
   // Launched with programmatic stream serialization (see abi.cu): this grid
@@ -523,7 +684,7 @@ __global__ void __launch_bounds__(kThreads, (W > 0 ? kBlocksPerSm : 2))
     const Seg& d = p.seg[s];
     const int64_t local = c - first;
     switch (d.kind) {
-      case kStep: step_chunk<W, kSplit>(p, d, local * kChunkElems); break;
+      case kStep: step_chunk<W, kSplit, kWithRealign>(p, d, local * kChunkElems); break;
       case kReduce: reduce_chunk<W, kSplit>(p, d, local * kChunkElems); break;
       case kAdam: adam_chunk<kSplit>(p, d, local * kChunkElems); break;
       case kCopy: bytes_chunk<false>(p, d, local * kChunkBytes); break;

@@ -297,7 +297,7 @@ __device__ __forceinline__ void tma_store_copy(const Params& p, const Seg& d, in
 template <int W>
 __device__ __noinline__ void tma_unstaged(const Params& p, const Seg& d, int64_t l) {
   switch (d.kind) {
-    case kStep: step_chunk<W, false>(p, d, l * kChunkElems); break;
+    case kStep: step_chunk<W, false, false>(p, d, l * kChunkElems); break;
     case kReduce: reduce_chunk<W, false>(p, d, l * kChunkElems); break;
     case kAdam: adam_chunk<false>(p, d, l * kChunkElems); break;
     case kCopy: bytes_chunk<false>(p, d, l * kChunkBytes); break;
@@ -382,7 +382,7 @@ __global__ void __launch_bounds__(kTmaThreads, (kInterleave && !kOutOfLine) ? 2 
       tma_unstaged<W>(p, d, l);
     } else {
       switch (d.kind) {
-        case kStep: step_chunk<W, false>(p, d, l * kChunkElems); break;
+        case kStep: step_chunk<W, false, false>(p, d, l * kChunkElems); break;
         case kReduce: reduce_chunk<W, false>(p, d, l * kChunkElems); break;
         case kAdam: adam_chunk<false>(p, d, l * kChunkElems); break;
         case kCopy: bytes_chunk<false>(p, d, l * kChunkBytes); break;

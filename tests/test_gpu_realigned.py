@@ -1,0 +1,113 @@
+"""Steps whose rows and outputs, or state, lie off 16-byte alignment by a common
+phase, against the oracle on every element.
+
+When a shard length S is not a multiple of 8 elements, position p's slice of
+every gradient row and of the gathered buffer starts 2pS bytes past a 16-byte
+boundary (mod 16), and a rank's state views start 4pS bytes past one when they
+are views of one buffer. The library gives such a step segment a width code
+with the two phases, and the LDG form reads its rows as aligned 16-byte blocks
+shifted into place and its state as aligned blocks shifted by whole words,
+instead of falling back to one element per thread. Cases: all ranks at W = 2,
+4, 8, 16 with the bench's buffers (rows of one (W, padded) buffer, state of one
+(R, padded) buffer per quantity), hybrid groups, the local-rank mode over units
+of odd sizes, and special values with every state phase (0, 4, 8, 12 bytes).
+"""
+import numpy as np
+import pytest
+
+import full_parity
+import gpu_util as gu
+import synth
+from synth import workloads as wls
+from test_gpu_special_values import _same_or_both_nan, _same_or_both_nan_bf16, _special_inputs
+
+pytestmark = pytest.mark.gpu
+
+fs = pytest.importorskip("fully_sharded_gb300")
+bench = pytest.importorskip("bench")
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _cuda():
+    torch = pytest.importorskip("torch")
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA GPU")
+    yield
+    torch.cuda.empty_cache()
+
+
+def _every_element(ora, wl, units, rb, re, step, what):
+    for u, unit in enumerate(units):
+        lay = unit["layout"]
+        regen = full_parity.state_regen(wl, u, lay.numel)(lay.shard_numel, lay.shard_factor)
+        assert full_parity.check_unit_every_element(ora, unit, rb, re, step, regen, "%s unit %d" % (what, u)) \
+            == lay.shard_numel
+
+
+@pytest.mark.parametrize("W,F", [(2, 2), (4, 4), (8, 8), (16, 16), (16, 4), (8, 2)])
+def test_odd_shards_all_ranks(ora, W, F):
+    """One FlatParameter whose shards are an odd number of elements long, every rank stepped
+    in one launch (the LDG form: the TMA form leaves launches made mostly of such segments)."""
+    torch = gu.torch()
+    # S odd; with groups (F < W) the padded length is a multiple of W, so S is a
+    # multiple of W / F: 4 times an odd number here
+    S = 300_001 if F == W else 4 * 75_001
+    n = F * S - 1
+    wl = bench.sweep_workload(n, W) if F == W else wls.Workload("odd_hybrid", 9, [[(n,)]], W, shard_factors=(F,),
+                                                                    sigma_state=1e-4)
+    units, info, keep = bench.build_all_ranks(wl, F, torch, fs, synth)
+    lay = units[0]["layout"]
+    assert lay.shard_numel == S and S % 8 != 0
+    launches, tma = fs.fsdp_shard_step_grouped_plan(units, 0, W)
+    assert (launches, tma) == (1, 0)
+    fs.fsdp_shard_step_grouped(units, 0, W, gu.adam_hyper(2))
+    torch.cuda.synchronize()
+    _every_element(ora, wl, units, 0, W, 2, "odd S, W=%d F=%d" % (W, F))
+    del units, keep
+
+
+def test_odd_units_local_rank(ora):
+    """The local-rank mode over units of odd sizes: each unit's rows, gathered slices and
+    state views (one buffer per quantity) start at their own phases."""
+    torch = gu.torch()
+    W, rank = 8, 5
+    sizes = [8 * 120_001 - 3, 8 * 200_003, 8 * 77_777 - 7, 8 * 300_000, 8 * 99_999 - 1]
+    wl = wls.Workload("odd_local", 7, [[(P,)] for P in sizes], W, sigma_state=1e-4)
+    units, info, bufs = bench.build_local_rank(wl, rank, torch, fs, synth)
+    fs.fsdp_shard_step_grouped(units, rank, rank + 1, gu.adam_hyper(7))
+    torch.cuda.synchronize()
+    _every_element(ora, wl, units, rank, rank + 1, 7, "odd local")
+    del units, bufs
+
+
+@pytest.mark.parametrize("state_off", [0, 1, 2, 3])
+def test_realigned_special_values(ora, state_off):
+    """Special values (infinities, NaN, subnormals, signed zeros, extreme masters) through the
+    realigned path, with every state phase: the state views start state_off elements (4 bytes
+    each) into their buffers; S is odd, so most positions' rows lie off alignment too."""
+    torch = gu.torch()
+    W = 4
+    S = 8193
+    P = W * S - 2
+    lay, _ = fs.fsdp_flatten_layout([P], W)
+    padded = lay.padded_numel
+    assert lay.shard_numel == S
+    grads, master, m, v = _special_inputs(np.random.default_rng(700 + state_off), W, P, padded)
+    sl = lambda a, r: a[r * S:(r + 1) * S].copy()  # noqa: E731
+    rows = torch.zeros((W, padded), dtype=torch.int16, device="cuda")
+    for k in range(W):
+        rows[k] = gu.to_dev(grads[k])
+    md = [gu.to_dev_at(sl(master, r), state_off) for r in range(W)]
+    ed = [gu.to_dev_at(sl(m, r), state_off) for r in range(W)]
+    vd = [gu.to_dev_at(sl(v, r), state_off) for r in range(W)]
+    full = torch.zeros(padded, dtype=torch.int16, device="cuda")
+    fs.fsdp_shard_step([rows[k] for k in range(W)], lay, 0, W, md, ed, vd, None, [full], gu.adam_hyper(3))
+    torch.cuda.synchronize()
+    om, oe, ov = [sl(master, r) for r in range(W)], [sl(m, r) for r in range(W)], [sl(v, r) for r in range(W)]
+    ofull = [np.zeros(padded, np.uint16)]
+    ora.shard_step(grads, W, 0, W, om, oe, ov, None, ofull, step=3, **gu.HP)
+    for r in range(W):
+        _same_or_both_nan(gu.to_host(md[r]), om[r], "master r%d" % r)
+        _same_or_both_nan(gu.to_host(ed[r]), oe[r], "exp_avg r%d" % r)
+        _same_or_both_nan(gu.to_host(vd[r]), ov[r], "exp_avg_sq r%d" % r)
+    _same_or_both_nan_bf16(gu.to_host(full), ofull[0], "full")

@@ -2,15 +2,15 @@
 
 The W = 16 instantiation of the TMA form (two 88 KB stages, one bulk copy per
 array) runs single-replica W = 16 launches whose gradient rows are not all a
-multiple of 2 KB apart. Each case draws units of random sizes (odd sizes put
-later units' state views and gathered shards off 16- and 32-byte alignment,
-which the form leaves to its unstaged path or stores as two float4), a mode
-(every rank stepped, or one rank stepped with the other 15 shards gathered), a
-step counter and Adam hyper-parameters; units are added until the launch holds
-enough chunks for the form. The rows are laid out off the 2 KB grain: in the
-all-ranks mode the first unit has an odd padded length (its rows, one per rank
-in a (16, padded) buffer, are a multiple of 32 bytes apart but not of 2 KB), in the
-local-rank mode the gradient pool's rows are an odd multiple of 1 KB apart.
+multiple of 2 KB apart. Each case draws units of random sizes (multiples of
+8 W, then one or two small units of odd sizes whose shards lie off alignment and
+take the form's unstaged path), a mode (every rank stepped, or one rank stepped
+with the other 15 shards gathered), a step counter and Adam hyper-parameters;
+units are added until the launch holds enough chunks for the form. The rows are
+laid out off the 2 KB grain: in the all-ranks mode the first unit's padded
+length is an odd multiple of 128 (its rows, one per rank in a (16, padded)
+buffer, are a multiple of 256 bytes apart but not of 2 KB), in the local-rank
+mode the gradient pool's rows are an odd multiple of 1 KB apart.
 Inputs are filled on the device by the seeded generator; every output of every
 unit is compared with the oracle's shard_step bit for bit (tests/full_parity.py).
 """
@@ -45,24 +45,28 @@ def _chunks(P, local):
 
 
 def _draw_units(rng, local, need_chunks):
-    """Units for one launch, the first one of an odd size off the 2 KB row grain, the last
-    one sized so that the launch reaches `need_chunks`. A launch's descriptor table holds
-    20 units of the local-rank step and 6 of the all-ranks step (16 segments of 20
-    pointers each) at W = 16: at most 16 and 6 units are drawn."""
-    k = int(rng.integers(1000, 200_000))
-    if (k + 1) % 64 == 0:
-        k += 1
-    units, chunks = [[(W * k + 7,)]], _chunks(W * k + 7, local)  # padded = 16 (k + 1), not a multiple of 1024
-    while chunks < need_chunks and len(units) < (15 if local else 5):
-        kind = int(rng.integers(0, 4))
-        P = int([rng.integers(1, 6000), rng.integers(6000, 2_000_000), rng.integers(2_000_000, 9_000_000),
+    """Units for one launch. Sizes are multiples of 8 W (shards of whole 16-byte rows), the
+    first one an odd multiple of 128 (its padded length is not a multiple of 1024: its
+    rows, one per rank in a (16, padded) buffer, are off the 2 KB grain), the last of them
+    sized so that the launch reaches `need_chunks`; then one or two small units of odd
+    sizes (shards off alignment). A launch's descriptor table holds 20 units of the
+    local-rank step and 6 of the all-ranks step (16 segments of 20 pointers each) at
+    W = 16: at most 16 and 6 units are drawn."""
+    k = int(rng.integers(100, 20_000)) | 1
+    units, chunks = [[(128 * k,)]], _chunks(128 * k, local)
+    while chunks < need_chunks and len(units) < (12 if local else 3):
+        kind = int(rng.integers(0, 3))
+        P = int([rng.integers(6000, 2_000_000), rng.integers(2_000_000, 9_000_000),
                  W * 2048 * rng.integers(1, 150)][kind])
+        P = -(-P // (8 * W)) * 8 * W
         units.append([(P,)])
         chunks += _chunks(P, local)
-    if chunks < need_chunks:  # one more unit, of an odd size, with the chunks still missing
+    if chunks < need_chunks:  # one more unit with the chunks still missing
         per_elem = (1 / 2048 + (W - 1) * 2 / 16384) / W if local else 1 / 2048
-        P = int((need_chunks - chunks) / per_elem * 1.05) | 1
+        P = -(-int((need_chunks - chunks) / per_elem * 1.05) // (8 * W)) * 8 * W
         units.append([(P,)])
+    for _ in range(int(rng.integers(1, 3))):
+        units.append([(int(rng.integers(1, 6000)) | 1,)])
     return units
 
 

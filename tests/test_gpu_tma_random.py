@@ -1,8 +1,8 @@
 """Random launches of the TMA form against the oracle, on every element.
 
-Each case draws a set of units (from a few elements to millions; odd sizes put
-the state views and gathered shards of later units off 16-byte alignment, which
-the TMA form leaves to its unstaged path), a mode (every rank stepped, or one
+Each case draws a set of units (thousands to millions of elements in multiples
+of 8 W, then a few small units of odd sizes whose shards lie off 16-byte
+alignment, which the TMA form leaves to its unstaged path), a mode (every rank stepped, or one
 rank stepped with the other ranks' shards gathered), a step counter and Adam
 hyper-parameters. Units are added until the launch holds enough chunks for the
 library to choose the TMA form (checked with the plan). Inputs are filled on
@@ -42,19 +42,25 @@ def _chunks(P, local):
 
 def _draw_units(rng, local, need_chunks):
     """Units for one launch: at most 18 of them (a launch's descriptor table holds 40 units
-    of the local-rank step and 21 of the all-ranks step), the last one sized so the
-    launch reaches `need_chunks`."""
+    of the local-rank step and 21 of the all-ranks step). Their sizes are multiples of 8 W
+    (shards of whole 16-byte rows) up to a last one that brings the launch to
+    `need_chunks`; then one to three small units of odd sizes, whose shards (and, in the
+    local-rank mode, the state views after them) lie off alignment. Launches made mostly
+    of such segments take the LDG form instead (tests/test_gpu_realigned.py)."""
     units, chunks = [], 0
-    while chunks < need_chunks and len(units) < 17:
-        kind = int(rng.integers(0, 4))
-        P = int([rng.integers(1, 6000), rng.integers(6000, 2_000_000), rng.integers(2_000_000, 9_000_000),
+    while chunks < need_chunks and len(units) < 14:
+        kind = int(rng.integers(0, 3))
+        P = int([rng.integers(6000, 2_000_000), rng.integers(2_000_000, 9_000_000),
                  W * 2048 * rng.integers(1, 300)][kind])
+        P = -(-P // (8 * W)) * 8 * W
         units.append([(P,)])
         chunks += _chunks(P, local)
-    if chunks < need_chunks:  # one more unit, of an odd size, with the chunks still missing
+    if chunks < need_chunks:  # one more unit with the chunks still missing
         per_elem = 22 / 16384 / W if local else 1 / 2048
-        P = int((need_chunks - chunks) / per_elem * 1.05) | 1
+        P = -(-int((need_chunks - chunks) / per_elem * 1.05) // (8 * W)) * 8 * W
         units.append([(P,)])
+    for _ in range(int(rng.integers(1, 4))):
+        units.append([(int(rng.integers(1, 6000)) | 1,)])
     return units
 
 
@@ -106,11 +112,12 @@ def _check_random_launch(ora, seed, local, row_numel=0):
 
 def test_grouped_launch_split_over_both_forms(ora):
     """45 local-rank units of 4 M elements: the grouped step needs two descriptor tables
-    (40 units of 8 segments each fit one); the first holds enough chunks for the TMA form,
-    the second (5 units) runs on the LDG form. Every element of every unit matches."""
+    (320 segments fit one); the first (every unit's step, then 275 gathers) holds enough
+    chunks for the TMA form, the second (the other 40 gathers) runs on the LDG form.
+    Every element of every unit matches."""
     torch = gu.torch()
     rng = np.random.default_rng(990)
-    sizes = [4_000_000 + int(rng.integers(0, 64)) for _ in range(45)]  # odd sizes: mixed alignment
+    sizes = [4_000_000 + 64 * int(rng.integers(0, 64)) for _ in range(45)]
     wl = wls.Workload("tma_split", 7, [[(P,)] for P in sizes], W, sigma_state=1e-4)
     rank, step = 5, 77
     units, info, bufs = bench.build_local_rank(wl, rank, torch, fs, synth)
