@@ -287,6 +287,7 @@ bool wants_split(const Params& p) {
   for (int k = 0; k < p.nseg; ++k) {
     const Seg& d = p.seg[k];
     if (d.kind == kAdam) {
+      if (d.width == kPhased) return false;  // the realigned path has the consecutive mapping
       any = true;
     } else if (d.kind == kStep) {
       if (2 * d.nrep < p.s.w) return false;
@@ -373,7 +374,7 @@ int launch(const SegmentList& list, const Scalars& s, cudaStream_t stream, int* 
       continue;
     }
     bool realign = false;
-    for (int k = 0; k < p.nseg; ++k) realign = realign || (p.seg[k].kind == kStep && p.seg[k].width == kPhased);
+    for (int k = 0; k < p.nseg; ++k) realign = realign || p.seg[k].width == kPhased;  // copy widths are <= 16
     if (realign) {
       const int cap = grid_capacity(variant + kRealignVariants, &err);
       if (err != FSDP_OK) return err;

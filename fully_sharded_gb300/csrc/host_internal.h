@@ -23,9 +23,9 @@ struct SegmentList {
   static bool aligned16(const void* q) { return (reinterpret_cast<uintptr_t>(q) & 15u) == 0; }
 
   // kStep / kReduce / kAdam: `ptrs` in pool order; width 16 iff all are aligned.
-  // A kStep segment with some pointer off 16-byte alignment but every pointer
-  // aligned to its element (2 bytes for rows and outputs, 4 for state) gets
-  // kPhased (the realigned vector path).
+  // A segment with some pointer off 16-byte alignment but every pointer aligned
+  // to its element (2 bytes for bf16, 4 for fp32) gets kPhased (the realigned
+  // vector path).
   void add_elementwise(SegKind kind, int64_t n, int nrep, const std::vector<const void*>& ptrs) {
     if (n <= 0) return;
     bool ok = true;
@@ -36,26 +36,43 @@ struct SegmentList {
     d.nrep = nrep;
     d.ptr = static_cast<int32_t>(ptr.size());
     d.width = ok ? 16 : 0;
-    if (!ok && kind == kStep) d.width = step_phases(nrep, ptrs);
+    if (!ok) d.width = phased_code(kind, nrep, ptrs);
     seg.push_back(d);
     ptr.insert(ptr.end(), ptrs.begin(), ptrs.end());
   }
 
-  // The width code of a step segment (not every pointer 16-byte aligned) whose
-  // pointers are all aligned to their elements: kPhased, else 0.
-  static int step_phases(int nrep, const std::vector<const void*>& ptrs) {
-    const size_t w = ptrs.size() - 4 * static_cast<size_t>(nrep);
-    if (nrep < 1 || w < 1 || w > ptrs.size()) return 0;
-    const auto low = [](const void* q) { return reinterpret_cast<uintptr_t>(q) & 15u; };
-    for (size_t k = 0; k < w; ++k)
-      if (!ptrs[k] || (low(ptrs[k]) & 1u)) return 0;
-    for (int r = 0; r < nrep; ++r) {
-      const size_t b = w + 4 * static_cast<size_t>(r);
-      for (int a = 0; a < 3; ++a)
-        if (!ptrs[b + a] || (low(ptrs[b + a]) & 3u)) return 0;
-      if (!ptrs[b + 3] || (low(ptrs[b + 3]) & 1u)) return 0;
+  // The width code of an elementwise segment (not every pointer 16-byte
+  // aligned) whose pointers are all aligned to their elements: kPhased, else 0.
+  // Pools: kStep W bf16 rows, then nrep x {3 fp32, bf16 out}; kReduce W bf16
+  // rows, fp32 out; kAdam fp32 grad, 3 fp32, bf16 out (may be null).
+  static int phased_code(SegKind kind, int nrep, const std::vector<const void*>& ptrs) {
+    const auto fits = [](const void* q, uintptr_t a) {  // non-null and aligned to a bytes
+      return q != nullptr && (reinterpret_cast<uintptr_t>(q) & (a - 1)) == 0;
+    };
+    if (kind == kStep) {
+      const size_t w = ptrs.size() - 4 * static_cast<size_t>(nrep);
+      if (nrep < 1 || w < 1 || w > ptrs.size()) return 0;
+      for (size_t k = 0; k < w; ++k)
+        if (!fits(ptrs[k], 2)) return 0;
+      for (int r = 0; r < nrep; ++r) {
+        const size_t b = w + 4 * static_cast<size_t>(r);
+        if (!fits(ptrs[b], 4) || !fits(ptrs[b + 1], 4) || !fits(ptrs[b + 2], 4) || !fits(ptrs[b + 3], 2)) return 0;
+      }
+      return kPhased;
     }
-    return kPhased;
+    if (kind == kReduce) {
+      if (ptrs.size() < 2) return 0;
+      for (size_t k = 0; k + 1 < ptrs.size(); ++k)
+        if (!fits(ptrs[k], 2)) return 0;
+      return fits(ptrs.back(), 4) ? kPhased : 0;
+    }
+    if (kind == kAdam) {
+      if (ptrs.size() != 5) return 0;
+      for (int a = 0; a < 4; ++a)
+        if (!fits(ptrs[a], 4)) return 0;
+      return (ptrs[4] == nullptr || fits(ptrs[4], 2)) ? kPhased : 0;
+    }
+    return 0;
   }
 
   void add_bytes(SegKind kind, const void* src, void* dst, int64_t bytes) {

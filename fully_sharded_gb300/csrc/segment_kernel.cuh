@@ -69,9 +69,9 @@ constexpr int kBlocksPerSm = 3;
 
 enum SegKind : int32_t { kStep = 0, kReduce = 1, kAdam = 2, kCopy = 3, kZero = 4 };
 
-// Width code of a step segment with some pointer off 16-byte alignment but every
-// pointer aligned to its element (2 bytes for rows and outputs, 4 for state):
-// its chunks take the realigned vector path.
+// Width code of a step, reduce or Adam segment with some pointer off 16-byte
+// alignment but every pointer aligned to its element (2 bytes for bf16, 4 for
+// fp32): its chunks take the realigned vector path.
 constexpr int32_t kPhased = 32;
 
 // One segment. Pointer pool layout (Params::ptr, starting at `ptr`):
@@ -88,7 +88,7 @@ struct Seg {
   int32_t nrep;       // kStep: replicas updated from the reduced gradient
   int32_t ptr;        // first pool entry
   int32_t width;      // kStep/kReduce/kAdam: 16 if every pointer is 16-byte aligned, else 0;
-                      // kStep also kPhased (see there);
+                      // kStep / kReduce / kAdam also kPhased (see there);
                       // kCopy/kZero: access width in bytes (16, 8, 4, 2 or 1)
 };
 
@@ -457,9 +457,14 @@ __device__ __forceinline__ void store_bf16_transposed(float* buf, uint16_t* q, c
 // elements pass the segment's end takes one element per lane. Same arithmetic
 // in the same order as the aligned path. Out of line, so that the aligned path
 // keeps its registers.
+// The warp's staging row (256 floats) of the realigned paths, one per warp.
+__device__ __forceinline__ float* realign_stage(int warp) {
+  __shared__ __align__(16) float stage[kThreads / 32][32 * kVec];
+  return stage[warp];
+}
+
 template <int W>
 __device__ __noinline__ void step_chunk_realigned(const Params& p, const Seg& d, int64_t e0) {
-  __shared__ __align__(16) float stage[kThreads / 32][32 * kVec];
   const int w = W > 0 ? W : p.s.w;
   const int warp = static_cast<int>(threadIdx.x / 32), lane = static_cast<int>(threadIdx.x % 32);
   const int64_t ew = e0 + int64_t(warp) * 32 * kVec;  // the warp's first element
@@ -476,7 +481,7 @@ __device__ __noinline__ void step_chunk_realigned(const Params& p, const Seg& d,
   load_f32x8_any(static_cast<const float*>(p.ptr[b0 + 2]) + e, st.v);
   float g[8];
   fold8_realigned<W>(p, d, e, g);
-  float* buf = stage[warp];
+  float* buf = realign_stage(warp);
   for (int r = 0; r < d.nrep; ++r) {
     const int b = b0 + 4 * r;
     float* mp = static_cast<float*>(const_cast<void*>(p.ptr[b]));
@@ -549,10 +554,34 @@ __device__ __forceinline__ void step_chunk(const Params& p, const Seg& d, int64_
   }
 }
 
-template <int W, bool kSplit>
+// A reduce chunk of a kPhased segment: rows realigned as in
+// step_chunk_realigned, the fp32 results stored through the warp's staging row.
+template <int W>
+__device__ __noinline__ void reduce_chunk_realigned(const Params& p, const Seg& d, int64_t e0) {
+  const int w = W > 0 ? W : p.s.w;
+  float* out = static_cast<float*>(const_cast<void*>(p.ptr[d.ptr + w]));
+  const int warp = static_cast<int>(threadIdx.x / 32), lane = static_cast<int>(threadIdx.x % 32);
+  const int64_t ew = e0 + int64_t(warp) * 32 * kVec;
+  if (ew >= d.n) return;
+  if (ew + 32 * kVec > d.n) {
+    for (int64_t i = ew + lane; i < d.n; i += 32) out[i] = fold1<W>(p, d, i);
+    return;
+  }
+  float g[8];
+  fold8_realigned<W>(p, d, ew + int64_t(lane) * kVec, g);
+  store_f32_transposed(realign_stage(warp), out + ew, g, lane);
+}
+
+template <int W, bool kSplit, bool kRealign = false>
 __device__ __forceinline__ void reduce_chunk(const Params& p, const Seg& d, int64_t e0) {
   const int w = W > 0 ? W : p.s.w;
   float* out = static_cast<float*>(const_cast<void*>(p.ptr[d.ptr + w]));
+  if constexpr (!kSplit && kRealign) {
+    if (d.width == kPhased) {
+      reduce_chunk_realigned<W>(p, d, e0);
+      return;
+    }
+  }
   if (d.width == 16) {
     constexpr int64_t o = Map<kSplit>::kSecond;
     const int64_t e = group_start<kSplit>(e0);
@@ -578,8 +607,52 @@ __device__ __forceinline__ void reduce_chunk(const Params& p, const Seg& d, int6
   }
 }
 
-template <bool kSplit>
+// An Adam chunk of a kPhased segment: gradient and state read as realigned
+// blocks, results stored through the warp's staging row.
+static __device__ __noinline__ void adam_chunk_realigned(const Params& p, const Seg& d, int64_t e0) {
+  const float* gp = static_cast<const float*>(p.ptr[d.ptr]);
+  float* mp = static_cast<float*>(const_cast<void*>(p.ptr[d.ptr + 1]));
+  float* mm = static_cast<float*>(const_cast<void*>(p.ptr[d.ptr + 2]));
+  float* mv = static_cast<float*>(const_cast<void*>(p.ptr[d.ptr + 3]));
+  uint16_t* out = static_cast<uint16_t*>(const_cast<void*>(p.ptr[d.ptr + 4]));
+  const int warp = static_cast<int>(threadIdx.x / 32), lane = static_cast<int>(threadIdx.x % 32);
+  const int64_t ew = e0 + int64_t(warp) * 32 * kVec;
+  if (ew >= d.n) return;
+  if (ew + 32 * kVec > d.n) {
+    for (int64_t i = ew + lane; i < d.n; i += 32) {
+      float pv = mp[i], mvv = mm[i], vv = mv[i];
+      adam1(gp[i], pv, mvv, vv, p.s);
+      mp[i] = pv;
+      mm[i] = mvv;
+      mv[i] = vv;
+      if (out) out[i] = bf16_rn(pv);
+    }
+    return;
+  }
+  const int64_t e = ew + int64_t(lane) * kVec;
+  float g[8];
+  State8 st;
+  load_f32x8_any(gp + e, g);
+  load_f32x8_any(mp + e, st.p);
+  load_f32x8_any(mm + e, st.m);
+  load_f32x8_any(mv + e, st.v);
+#pragma unroll
+  for (int i = 0; i < 8; ++i) adam1(g[i], st.p[i], st.m[i], st.v[i], p.s);
+  float* buf = realign_stage(warp);
+  store_f32_transposed(buf, mp + ew, st.p, lane);
+  store_f32_transposed(buf, mm + ew, st.m, lane);
+  store_f32_transposed(buf, mv + ew, st.v, lane);
+  if (out) store_bf16_transposed(buf, out + ew, st.p, lane);
+}
+
+template <bool kSplit, bool kRealign = false>
 __device__ __forceinline__ void adam_chunk(const Params& p, const Seg& d, int64_t e0) {
+  if constexpr (!kSplit && kRealign) {
+    if (d.width == kPhased) {
+      adam_chunk_realigned(p, d, e0);
+      return;
+    }
+  }
   const float* gp = static_cast<const float*>(p.ptr[d.ptr]);
   float* mp = static_cast<float*>(const_cast<void*>(p.ptr[d.ptr + 1]));
   float* mm = static_cast<float*>(const_cast<void*>(p.ptr[d.ptr + 2]));
@@ -685,8 +758,8 @@ __global__ void __launch_bounds__(kThreads, (W > 0 ? kBlocksPerSm : 2))
     const int64_t local = c - first;
     switch (d.kind) {
       case kStep: step_chunk<W, kSplit, kWithRealign>(p, d, local * kChunkElems); break;
-      case kReduce: reduce_chunk<W, kSplit>(p, d, local * kChunkElems); break;
-      case kAdam: adam_chunk<kSplit>(p, d, local * kChunkElems); break;
+      case kReduce: reduce_chunk<W, kSplit, kWithRealign>(p, d, local * kChunkElems); break;
+      case kAdam: adam_chunk<kSplit, kWithRealign>(p, d, local * kChunkElems); break;
       case kCopy: bytes_chunk<false>(p, d, local * kChunkBytes); break;
       default: bytes_chunk<true>(p, d, local * kChunkBytes); break;
     }

@@ -10,7 +10,8 @@ shifted into place and its state as aligned blocks shifted by whole words,
 instead of falling back to one element per thread. Cases: all ranks at W = 2,
 4, 8, 16 with the bench's buffers (rows of one (W, padded) buffer, state of one
 (R, padded) buffer per quantity), hybrid groups, the local-rank mode over units
-of odd sizes, and special values with every state phase (0, 4, 8, 12 bytes).
+of odd sizes, special values with every state phase (0, 4, 8, 12 bytes), and
+the one-launch reduce-scatter and grouped Adam on arrays at their own phases.
 """
 import numpy as np
 import pytest
@@ -111,3 +112,62 @@ def test_realigned_special_values(ora, state_off):
         _same_or_both_nan(gu.to_host(ed[r]), oe[r], "exp_avg r%d" % r)
         _same_or_both_nan(gu.to_host(vd[r]), ov[r], "exp_avg_sq r%d" % r)
     _same_or_both_nan_bf16(gu.to_host(full), ofull[0], "full")
+
+
+@pytest.mark.parametrize("W", [4, 8, 16])
+def test_realigned_reduce_scatter(ora, W):
+    """Every rank's reduce-scatter in one launch with an odd S: each rank's slice of the rows
+    and its fp32 output (views of one buffer, at r S elements) lie at their own phases."""
+    torch = gu.torch()
+    S = 70_001
+    P = W * S - 1
+    lay, _ = fs.fsdp_flatten_layout([P], W)
+    padded = lay.padded_numel
+    assert lay.shard_numel == S
+    rng = np.random.default_rng(800 + W)
+    grads = [((rng.standard_normal(padded, dtype=np.float32) * 1e-2).view(np.uint32) >> 16).astype(np.uint16)
+             for _ in range(W)]
+    for g in grads:
+        g[P:] = 0
+    rows = torch.zeros((W, padded), dtype=torch.int16, device="cuda")
+    for k in range(W):
+        rows[k] = gu.to_dev(grads[k])
+    outs = torch.full((W * S,), float("nan"), device="cuda")
+    fs.fsdp_reduce_scatter_ranks([rows[k] for k in range(W)], lay, 0, W, [outs[r * S:(r + 1) * S] for r in range(W)])
+    torch.cuda.synchronize()
+    got = gu.to_host(outs)
+    for r in range(W):
+        gu.assert_same_bits(got[r * S:(r + 1) * S], ora.reduce_scatter(grads, W, r), "reduce-scatter r%d" % r)
+
+
+@pytest.mark.parametrize("offs", [(1, 2, 3, 1, 0), (0, 0, 0, 0, 1), (3, 1, 2, 2, 3)])
+def test_realigned_adam_grouped(ora, offs):
+    """Adam alone over shards whose gradient, state and bf16 output start at their own offsets
+    (elements) into their buffers, with special values: every non-NaN output bit-identical."""
+    torch = gu.torch()
+    rng = np.random.default_rng(900 + sum(offs))
+    specials = np.array([np.inf, -np.inf, np.nan, 0.0, -0.0, 1e-40, -1e-40, 3.3e38, -3.3e38, 1e-3],
+                        dtype=np.float32)
+    shards, want = [], []
+    for n in (100_003, 65_536 + 5):
+        g = (rng.standard_normal(n) * 1e-2).astype(np.float32)
+        idx = rng.choice(n, size=n // 16, replace=False)
+        g[idx] = rng.choice(specials, size=idx.size)
+        p = (rng.standard_normal(n) * 0.02).astype(np.float32)
+        m = np.abs(rng.standard_normal(n) * 1e-4).astype(np.float32)
+        v = np.abs(rng.standard_normal(n) * 1e-4).astype(np.float32)
+        v[rng.choice(n, size=n // 32, replace=False)] = 0.0
+        op, om, ov = p.copy(), m.copy(), v.copy()
+        obf = ora.adam(op, om, ov, g, step=4, **gu.HP)
+        want.append((op, om, ov, obf))
+        out_buf = torch.zeros(n + offs[4], dtype=torch.int16, device="cuda")
+        shards.append(dict(master=gu.to_dev_at(p, offs[0]), exp_avg=gu.to_dev_at(m, offs[1]),
+                           exp_avg_sq=gu.to_dev_at(v, offs[2]), grad_shard=gu.to_dev_at(g, offs[3]),
+                           bf16_shard_out=out_buf[offs[4]:], n=n))
+    fs.fsdp_adam_shard_step_grouped(shards, gu.adam_hyper(4))
+    torch.cuda.synchronize()
+    for i, (s, (op, om, ov, obf)) in enumerate(zip(shards, want)):
+        _same_or_both_nan(gu.to_host(s["master"]), op, "master %d" % i)
+        _same_or_both_nan(gu.to_host(s["exp_avg"]), om, "exp_avg %d" % i)
+        _same_or_both_nan(gu.to_host(s["exp_avg_sq"]), ov, "exp_avg_sq %d" % i)
+        _same_or_both_nan_bf16(gu.to_host(s["bf16_shard_out"]), obf, "bf16 %d" % i)
