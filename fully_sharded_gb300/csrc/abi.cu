@@ -233,7 +233,7 @@ bool rows_off_grain(const Params& p) {
 // 24 warps per SM carry such chunks better than the TMA form's 8 consumers.
 bool use_tma(const Params& p, int tma_grid) {
   bool step = false, copy = false;
-  int64_t step_chunks = 0, phased_chunks = 0;
+  int64_t step_chunks = 0, phased_chunks = 0, copy_chunks = 0, narrow_chunks = 0;
   for (int k = 0; k < p.nseg; ++k) {
     const Seg& d = p.seg[k];
     if (d.kind == kStep) {
@@ -243,6 +243,9 @@ bool use_tma(const Params& p, int tma_grid) {
       if (d.width == kPhased) phased_chunks += c;
       step = true;
     } else if (d.kind == kCopy) {
+      const int64_t c = (d.n + kChunkBytes - 1) / kChunkBytes;
+      copy_chunks += c;
+      if (d.width != 16) narrow_chunks += c;
       copy = true;
     } else if (d.kind != kZero) {
       return false;
@@ -259,6 +262,9 @@ bool use_tma(const Params& p, int tma_grid) {
   } else if (!copy) {
     return false;
   }
+  // likewise copies whose source and destination are not both 16-byte aligned
+  // (the TMA form copies them on the narrow path, the LDG form realigns them)
+  if (narrow_chunks * 8 > copy_chunks) return false;
   return p.total_chunks >=
          static_cast<int64_t>(step ? kTmaMinStepChunksPerBlock : kTmaMinChunksPerBlock) * tma_grid;
 }
@@ -374,7 +380,11 @@ int launch(const SegmentList& list, const Scalars& s, cudaStream_t stream, int* 
       continue;
     }
     bool realign = false;
-    for (int k = 0; k < p.nseg; ++k) realign = realign || p.seg[k].width == kPhased;  // copy widths are <= 16
+    for (int k = 0; k < p.nseg; ++k) {
+      const Seg& d = p.seg[k];
+      const bool bytes = d.kind == kCopy || d.kind == kZero;
+      realign = realign || (bytes ? d.width != 16 : d.width == kPhased);
+    }
     if (realign) {
       const int cap = grid_capacity(variant + kRealignVariants, &err);
       if (err != FSDP_OK) return err;

@@ -687,8 +687,74 @@ __device__ __forceinline__ void adam_chunk(const Params& p, const Seg& d, int64_
   }
 }
 
+// 16 bytes that start `phase` bytes (1..15) past the 16-byte boundary `al`,
+// from the aligned blocks at al and al + 16 (shifts by whole words, then by
+// whole bytes; the reads stay within the pages of the bytes used).
+__device__ __forceinline__ uint4 load_bytes_realigned(const unsigned char* al, int phase) {
+  const uint4 lo = ld_stream_u4(al), hi = ld_stream_u4(al + 16);
+  uint32_t w[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
+  const bool by2 = (phase & 8) != 0, by1 = (phase & 4) != 0;
+#pragma unroll
+  for (int i = 0; i < 6; ++i) w[i] = by2 ? w[i + 2] : w[i];
+#pragma unroll
+  for (int i = 0; i < 5; ++i) w[i] = by1 ? w[i + 1] : w[i];
+  const uint32_t h = static_cast<uint32_t>(phase & 3) * 8u;
+  return make_uint4(__funnelshift_r(w[0], w[1], h), __funnelshift_r(w[1], w[2], h), __funnelshift_r(w[2], w[3], h),
+                    __funnelshift_r(w[3], w[4], h));
+}
+
+// A copy (or zero-fill) chunk whose source and destination are not both 16-byte
+// aligned: every 16-byte block of the destination that lies inside the chunk is
+// written with one aligned store (its source bytes read as two aligned blocks
+// and shifted into place), the chunk's first and last bytes around them one
+// byte at a time (those blocks are shared with the neighbouring chunks).
 template <bool kZeroFill>
+__device__ __noinline__ void bytes_chunk_realigned(const Params& p, const Seg& d, int64_t b0) {
+  const unsigned char* src = kZeroFill ? nullptr : static_cast<const unsigned char*>(p.ptr[d.ptr]);
+  unsigned char* dst = static_cast<unsigned char*>(const_cast<void*>(p.ptr[d.ptr + (kZeroFill ? 0 : 1)]));
+  const int64_t end = (b0 + kChunkBytes < d.n) ? b0 + kChunkBytes : d.n;
+  const uintptr_t ds = reinterpret_cast<uintptr_t>(dst) + static_cast<uintptr_t>(b0);
+  const uintptr_t de = reinterpret_cast<uintptr_t>(dst) + static_cast<uintptr_t>(end);
+  const uintptr_t a = (ds + 15) & ~uintptr_t(15), z = de & ~uintptr_t(15);
+  if (a >= z) {
+    for (int64_t q = b0 + threadIdx.x; q < end; q += kThreads) dst[q] = kZeroFill ? 0 : src[q];
+    return;
+  }
+  const int64_t head = static_cast<int64_t>(a - ds), tail = static_cast<int64_t>(de - z);
+  if (int64_t(threadIdx.x) < head) dst[b0 + threadIdx.x] = kZeroFill ? 0 : src[b0 + threadIdx.x];
+  if (int64_t(threadIdx.x) < tail) {
+    const int64_t q = end - tail + threadIdx.x;
+    dst[q] = kZeroFill ? 0 : src[q];
+  }
+  // at most kThreads * kCopyVecs blocks: all loads first, then the stores
+  const int64_t nblk = static_cast<int64_t>(z - a) / 16;
+  const int64_t first = b0 + head;  // segment byte offset of the first whole block
+  const int py = kZeroFill ? 0 : static_cast<int>((reinterpret_cast<uintptr_t>(src) + first) & 15u);
+  uint4 v[kCopyVecs];
+#pragma unroll
+  for (int k = 0; k < kCopyVecs; ++k) {
+    const int64_t i = int64_t(k) * kThreads + threadIdx.x;
+    v[k] = make_uint4(0, 0, 0, 0);
+    if (!kZeroFill && i < nblk) {
+      const unsigned char* y = src + first + 16 * i;
+      v[k] = py == 0 ? ld_stream_u4(y) : load_bytes_realigned(y - py, py);
+    }
+  }
+#pragma unroll
+  for (int k = 0; k < kCopyVecs; ++k) {
+    const int64_t i = int64_t(k) * kThreads + threadIdx.x;
+    if (i < nblk) st_stream_u4(dst + first + 16 * i, v[k]);
+  }
+}
+
+template <bool kZeroFill, bool kRealign = false>
 __device__ __forceinline__ void bytes_chunk(const Params& p, const Seg& d, int64_t b0) {
+  if constexpr (kRealign) {
+    if (d.width != 16) {
+      bytes_chunk_realigned<kZeroFill>(p, d, b0);
+      return;
+    }
+  }
   const unsigned char* src =
       kZeroFill ? nullptr : static_cast<const unsigned char*>(p.ptr[d.ptr]);
   unsigned char* dst = static_cast<unsigned char*>(const_cast<void*>(p.ptr[d.ptr + (kZeroFill ? 0 : 1)]));
@@ -736,8 +802,9 @@ __device__ __forceinline__ void bytes_chunk(const Params& p, const Seg& d, int64
 
 // -------------------------------------------------------------- the kernel
 
-// kWithRealign: the instantiation for launches that hold kPhased step segments
-// (the consecutive mapping, with the realigned path).
+// kWithRealign: the instantiation for launches that hold kPhased segments or
+// copies off 16-byte alignment (the consecutive mapping, with the realigned
+// paths).
 template <int W, bool kSplit, bool kWithRealign = false>
 __global__ void __launch_bounds__(kThreads, (W > 0 ? kBlocksPerSm : 2))
     segment_kernel(const __grid_constant__ Params p) {
@@ -760,8 +827,8 @@ __global__ void __launch_bounds__(kThreads, (W > 0 ? kBlocksPerSm : 2))
       case kStep: step_chunk<W, kSplit, kWithRealign>(p, d, local * kChunkElems); break;
       case kReduce: reduce_chunk<W, kSplit, kWithRealign>(p, d, local * kChunkElems); break;
       case kAdam: adam_chunk<kSplit, kWithRealign>(p, d, local * kChunkElems); break;
-      case kCopy: bytes_chunk<false>(p, d, local * kChunkBytes); break;
-      default: bytes_chunk<true>(p, d, local * kChunkBytes); break;
+      case kCopy: bytes_chunk<false, kWithRealign>(p, d, local * kChunkBytes); break;
+      default: bytes_chunk<true, kWithRealign>(p, d, local * kChunkBytes); break;
     }
   }
 }

@@ -11,7 +11,9 @@ instead of falling back to one element per thread. Cases: all ranks at W = 2,
 4, 8, 16 with the bench's buffers (rows of one (W, padded) buffer, state of one
 (R, padded) buffer per quantity), hybrid groups, the local-rank mode over units
 of odd sizes, special values with every state phase (0, 4, 8, 12 bytes), and
-the one-launch reduce-scatter and grouped Adam on arrays at their own phases.
+the one-launch reduce-scatter and grouped Adam on arrays at their own phases,
+and copies (pack, unpack, all-gather) whose sources and destinations start at
+their own byte phases.
 """
 import numpy as np
 import pytest
@@ -171,3 +173,58 @@ def test_realigned_adam_grouped(ora, offs):
         _same_or_both_nan(gu.to_host(s["exp_avg"]), om, "exp_avg %d" % i)
         _same_or_both_nan(gu.to_host(s["exp_avg_sq"]), ov, "exp_avg_sq %d" % i)
         _same_or_both_nan_bf16(gu.to_host(s["bf16_shard_out"]), obf, "bf16 %d" % i)
+
+
+def _at(torch, h, off, dtype, pattern):
+    """A device copy of `h` that starts `off` elements into a buffer filled with `pattern`
+    (8 canary elements after it); returns (buffer, view)."""
+    buf = torch.full((off + h.size + 8,), pattern, dtype=dtype, device="cuda")
+    view = buf[off:off + h.size]
+    if h.size:
+        view.copy_(torch.from_numpy(np.ascontiguousarray(h).view(np.int16 if dtype == torch.int16 else np.float32)))
+    return buf, view
+
+
+def _canaries(buf, off, n, pattern):
+    h = buf.cpu()
+    return bool((h[:off] == pattern).all() and (h[off + n:] == pattern).all())
+
+
+@pytest.mark.parametrize("seed", range(3))
+def test_realigned_copies(ora, seed):
+    """Pack, unpack and all-gather of bf16 tensors whose sources and destinations start at
+    their own byte phases (element offsets 0..7 into their buffers): the copy segments go
+    to the realigned copy path (aligned 16-byte stores, sources shifted into place, the
+    bytes around them one at a time), the padding's zero fill too. Sizes from one element
+    to several chunks; canaries around every destination catch stray writes."""
+    torch = gu.torch()
+    rng = np.random.default_rng(1000 + seed)
+    numels = [1, 7, 15, 8191, 100_003, 3 * 8192 + 5, 0, 12_345, int(rng.integers(1, 40_000))]
+    W = 8
+    lay, offs = fs.fsdp_flatten_layout(numels, W)
+    hs = [rng.integers(0, 1 << 16, size=n, dtype=np.uint16) for n in numels]
+    src = [_at(torch, h, int(rng.integers(0, 8)), torch.int16, 5) for h in hs]
+    fo = int(rng.integers(1, 8))
+    fbuf, flat = _at(torch, np.zeros(lay.padded_numel, np.uint16), fo, torch.int16, 77)
+    flat.fill_(77)
+    fs.fsdp_pack_flat([v for _, v in src], lay, offs, flat)
+    gu.assert_same_bits(gu.to_host(flat), ora.pack(hs, lay.padded_numel), "pack")
+    assert _canaries(fbuf, fo, lay.padded_numel, 77), "write outside the flat buffer"
+    outs = [_at(torch, np.zeros(n, np.uint16), int(rng.integers(0, 8)), torch.int16, 9) for n in numels]
+    for _, v in outs:
+        v.fill_(9)
+    fs.fsdp_unpack_flat(flat, lay, offs, [v for _, v in outs])
+    for (b, v), h in zip(outs, hs):
+        gu.assert_same_bits(gu.to_host(v), h, "unpack of %d elements" % h.size)
+        assert _canaries(b, b.numel() - 8 - h.size, h.size, 9), "write outside an unpacked tensor"
+    # all-gather: odd shard length, each shard at its own offset, the full buffer at another
+    S = 50_001 + 2 * int(rng.integers(0, 1000))
+    glay, _ = fs.fsdp_flatten_layout([W * S], W)
+    shards = [rng.integers(0, 1 << 16, size=S, dtype=np.uint16) for _ in range(W)]
+    sd = [_at(torch, s, int(rng.integers(0, 8)), torch.int16, 3)[1] for s in shards]
+    go = int(rng.integers(0, 8))
+    gbuf, full = _at(torch, np.zeros(W * S, np.uint16), go, torch.int16, 11)
+    full.fill_(11)
+    fs.fsdp_all_gather(sd, glay, full)
+    gu.assert_same_bits(gu.to_host(full), ora.all_gather(shards), "all-gather")
+    assert _canaries(gbuf, go, W * S, 11), "write outside the full buffer"
