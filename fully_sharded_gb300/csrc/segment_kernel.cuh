@@ -232,38 +232,34 @@ __device__ __forceinline__ void add_row(float (&acc)[8], const RowLoad<kSplit>& 
   }
 }
 
-// The 8 bf16 values that start `phase` bytes (2..14, even) past the 16-byte
-// boundary `al`, from the two aligned 16-byte blocks at al and al + 16: a shift
-// by whole words (phase / 4, by selects on its two bits: the phase is the same
-// for every thread of a row) and then by half a word. The 32 bytes read stay within the pages
-// of the 16 bytes used (page boundaries are 16-byte aligned).
-__device__ __forceinline__ uint4 load_row_realigned(const unsigned char* al, int phase) {
-  const uint4 lo = ld_stream_u4(al), hi = ld_stream_u4(al + 16);
+// The 16 bytes that start `phase` bytes (0..15) into the aligned block lo, hi
+// being the aligned block after it: a shift by whole words (phase / 4, by
+// selects on its two bits: the phase is the same for every thread of a row or
+// array) and then by whole bytes.
+__device__ __forceinline__ uint4 shift_bytes(const uint4& lo, const uint4& hi, int phase) {
   uint32_t w[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
   const bool by2 = (phase & 8) != 0, by1 = (phase & 4) != 0;
 #pragma unroll
   for (int i = 0; i < 6; ++i) w[i] = by2 ? w[i + 2] : w[i];
 #pragma unroll
   for (int i = 0; i < 5; ++i) w[i] = by1 ? w[i + 1] : w[i];
-  const uint32_t h = (phase & 2) ? 16u : 0u;
+  const uint32_t h = static_cast<uint32_t>(phase & 3) * 8u;
   return make_uint4(__funnelshift_r(w[0], w[1], h), __funnelshift_r(w[1], w[2], h), __funnelshift_r(w[2], w[3], h),
                     __funnelshift_r(w[3], w[4], h));
 }
 
-// 8 fp32 values that start `phase` bytes (4, 8 or 12) past the 16-byte boundary
-// `al`, from the three aligned 16-byte blocks from al on (the same shifts by
-// whole words as load_row_realigned; the reads stay within the pages of the
-// 32 bytes used).
-__device__ __forceinline__ void load_f32x8_realigned(const float* al, int phase, float (&x)[8]) {
-  const float4 a = ld_stream_f4(al), b = ld_stream_f4(al + 4), c = ld_stream_f4(al + 8);
-  float w[12] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w, c.x, c.y, c.z, c.w};
-  const bool by2 = (phase & 8) != 0, by1 = (phase & 4) != 0;
-#pragma unroll
-  for (int i = 0; i < 10; ++i) w[i] = by2 ? w[i + 2] : w[i];
-#pragma unroll
-  for (int i = 0; i < 9; ++i) w[i] = by1 ? w[i + 1] : w[i];
-#pragma unroll
-  for (int i = 0; i < 8; ++i) x[i] = w[i];
+// The aligned 16-byte block that holds the first of the 16 bytes at x, and the
+// block after it (the same block again when x is aligned), for shift_bytes:
+// every block read holds one of the bytes used, so the reads stay within their
+// pages. Branch-free, so that a caller's loads of several rows are all in
+// flight before the first shift (measured on GB300: a branch on the phase, or
+// the second load predicated on it, kept fewer loads in flight and ran 4-20 %
+// slower).
+__device__ __forceinline__ void load_blocks(const void* x, uint4& lo, uint4& hi, int& phase) {
+  phase = static_cast<int>(reinterpret_cast<uintptr_t>(x) & 15u);
+  const unsigned char* al = static_cast<const unsigned char*>(x) - phase;
+  lo = ld_stream_u4(al);
+  hi = ld_stream_u4(al + (phase != 0 ? 16 : 0));
 }
 
 // fold8 (consecutive mapping) for rows at any even byte phase: each row's
@@ -274,20 +270,18 @@ __device__ __forceinline__ void fold8_realigned(const Params& p, const Seg& d, i
 #pragma unroll
   for (int i = 0; i < 8; ++i) g[i] = 0.0f;
   const int w = W > 0 ? W : p.s.w;
-  constexpr int kBatch = (W > 0 && W < 8) ? W : 8;
+  // rows loaded before they are shifted and added (8 at W >= 8; 4 for a
+  // runtime W, whose instantiation would spill more with 8)
+  constexpr int kBatch = W == 0 ? 4 : (W < 8 ? W : 8);
   for (int k0 = 0; k0 < w; k0 += kBatch) {
-    uint4 r[kBatch];
+    uint4 lo[kBatch], hi[kBatch];
+    int ph[kBatch];
 #pragma unroll
     for (int k = 0; k < kBatch; ++k)
-      if (W > 0 || k0 + k < w) {
-        const uint16_t* row = static_cast<const uint16_t*>(p.ptr[d.ptr + k0 + k]) + e;
-        const int phase = static_cast<int>(reinterpret_cast<uintptr_t>(row) & 15u);
-        r[k] = phase == 0 ? ld_stream_u4(row)
-                          : load_row_realigned(reinterpret_cast<const unsigned char*>(row) - phase, phase);
-      }
+      if (W > 0 || k0 + k < w) load_blocks(static_cast<const uint16_t*>(p.ptr[d.ptr + k0 + k]) + e, lo[k], hi[k], ph[k]);
 #pragma unroll
     for (int k = 0; k < kBatch; ++k)
-      if (W > 0 || k0 + k < w) add_bf16x8(g, r[k]);
+      if (W > 0 || k0 + k < w) add_bf16x8(g, shift_bytes(lo[k], hi[k], ph[k]));
   }
 #pragma unroll
   for (int i = 0; i < 8; ++i) g[i] = mean_of<W>(g[i], p.s);
@@ -417,15 +411,21 @@ __device__ __forceinline__ void step_scalar(const Params& p, const Seg& d, int64
 
 // The state of a thread's 8 elements from arrays at any 4-byte phase (each
 // array's own, read from its pointer).
+// Three aligned blocks from the one holding q[0] (at phase 0 the third is the
+// second again: every block read holds one of the 32 bytes used), shifted by
+// whole words; branch-free like load_blocks.
 __device__ __forceinline__ void load_f32x8_any(const float* q, float (&x)[8]) {
   const int phase = static_cast<int>(reinterpret_cast<uintptr_t>(q) & 15u);
-  if (phase == 0) {
-    const float4 a = ld_stream_f4(q), b = ld_stream_f4(q + 4);
-    x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
-    x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
-  } else {
-    load_f32x8_realigned(q - phase / 4, phase, x);
-  }
+  const float* al = q - phase / 4;
+  const float4 a = ld_stream_f4(al), b = ld_stream_f4(al + 4), c = ld_stream_f4(al + (phase != 0 ? 8 : 4));
+  float w[12] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w, c.x, c.y, c.z, c.w};
+  const bool by2 = (phase & 8) != 0, by1 = (phase & 4) != 0;
+#pragma unroll
+  for (int i = 0; i < 10; ++i) w[i] = by2 ? w[i + 2] : w[i];
+#pragma unroll
+  for (int i = 0; i < 9; ++i) w[i] = by1 ? w[i + 1] : w[i];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) x[i] = w[i];
 }
 
 // A warp's 256 results of one array, thread `lane` holding elements 8 lane ..
@@ -687,22 +687,6 @@ __device__ __forceinline__ void adam_chunk(const Params& p, const Seg& d, int64_
   }
 }
 
-// 16 bytes that start `phase` bytes (1..15) past the 16-byte boundary `al`,
-// from the aligned blocks at al and al + 16 (shifts by whole words, then by
-// whole bytes; the reads stay within the pages of the bytes used).
-__device__ __forceinline__ uint4 load_bytes_realigned(const unsigned char* al, int phase) {
-  const uint4 lo = ld_stream_u4(al), hi = ld_stream_u4(al + 16);
-  uint32_t w[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
-  const bool by2 = (phase & 8) != 0, by1 = (phase & 4) != 0;
-#pragma unroll
-  for (int i = 0; i < 6; ++i) w[i] = by2 ? w[i + 2] : w[i];
-#pragma unroll
-  for (int i = 0; i < 5; ++i) w[i] = by1 ? w[i + 1] : w[i];
-  const uint32_t h = static_cast<uint32_t>(phase & 3) * 8u;
-  return make_uint4(__funnelshift_r(w[0], w[1], h), __funnelshift_r(w[1], w[2], h), __funnelshift_r(w[2], w[3], h),
-                    __funnelshift_r(w[3], w[4], h));
-}
-
 // A copy (or zero-fill) chunk whose source and destination are not both 16-byte
 // aligned: every 16-byte block of the destination that lies inside the chunk is
 // written with one aligned store (its source bytes read as two aligned blocks
@@ -726,24 +710,28 @@ __device__ __noinline__ void bytes_chunk_realigned(const Params& p, const Seg& d
     const int64_t q = end - tail + threadIdx.x;
     dst[q] = kZeroFill ? 0 : src[q];
   }
-  // at most kThreads * kCopyVecs blocks: all loads first, then the stores
+  // at most kThreads * kCopyVecs blocks: all loads first (the source's aligned
+  // block holding the first byte and, off its boundary, the block after it;
+  // at phase 0 the same block twice), then the shifts and stores
   const int64_t nblk = static_cast<int64_t>(z - a) / 16;
   const int64_t first = b0 + head;  // segment byte offset of the first whole block
   const int py = kZeroFill ? 0 : static_cast<int>((reinterpret_cast<uintptr_t>(src) + first) & 15u);
-  uint4 v[kCopyVecs];
+  const int64_t next = py != 0 ? 16 : 0;
+  uint4 lo[kCopyVecs], hi[kCopyVecs];
 #pragma unroll
   for (int k = 0; k < kCopyVecs; ++k) {
     const int64_t i = int64_t(k) * kThreads + threadIdx.x;
-    v[k] = make_uint4(0, 0, 0, 0);
+    lo[k] = hi[k] = make_uint4(0, 0, 0, 0);
     if (!kZeroFill && i < nblk) {
-      const unsigned char* y = src + first + 16 * i;
-      v[k] = py == 0 ? ld_stream_u4(y) : load_bytes_realigned(y - py, py);
+      const unsigned char* al = src + first + 16 * i - py;
+      lo[k] = ld_stream_u4(al);
+      hi[k] = ld_stream_u4(al + next);
     }
   }
 #pragma unroll
   for (int k = 0; k < kCopyVecs; ++k) {
     const int64_t i = int64_t(k) * kThreads + threadIdx.x;
-    if (i < nblk) st_stream_u4(dst + first + 16 * i, v[k]);
+    if (i < nblk) st_stream_u4(dst + first + 16 * i, kZeroFill ? lo[k] : shift_bytes(lo[k], hi[k], py));
   }
 }
 
