@@ -530,6 +530,8 @@ using namespace fsdp;
 
 namespace {
 
+constexpr int64_t kSplitMinChunksPerSm = 256;  // see the split in grouped()
+
 int grouped(const fsdp_unit_args_t* units, int32_t n_units, int32_t rank_begin, int32_t rank_end,
             const fsdp_adam_t* adam, cudaStream_t stream, int* count, int* tma_count = nullptr,
             int* interleaved_count = nullptr) {
@@ -564,16 +566,54 @@ int grouped(const fsdp_unit_args_t* units, int32_t n_units, int32_t rank_begin, 
   // 8.562 -> 8.471 ms (two boxes), four Llama blocks 1.031 -> 1.006 ms, GPT-2
   // small 0.173 -> 0.165 ms; the gathers first instead were 2 % slower than this
   // on the last two and equal on the 7B step.
-  SegmentList ordered;
+  SegmentList ordered, aligned, off;
   for (int pass = 0; pass < 2; ++pass) {
     for (size_t i = 0; i < list.seg.size(); ++i) {
       const Seg& d = list.seg[i];
       if ((pass == 0) != (d.kind == kStep)) continue;
-      Seg e = d;
-      e.ptr = static_cast<int32_t>(ordered.ptr.size());
-      ordered.seg.push_back(e);
-      const int np = list.pool_size(i);
-      for (int k = 0; k < np; ++k) ordered.ptr.push_back(list.ptr[d.ptr + k]);
+      const bool phased = d.kind == kCopy ? d.width != 16 : d.width == kPhased;
+      for (SegmentList* to : {&ordered, phased ? &off : &aligned}) {
+        Seg e = d;
+        e.ptr = static_cast<int32_t>(to->ptr.size());
+        to->seg.push_back(e);
+        const int np = list.pool_size(i);
+        for (int k = 0; k < np; ++k) to->ptr.push_back(list.ptr[d.ptr + k]);
+      }
+    }
+  }
+  // A launch that holds too many segments off alignment for the TMA form (its
+  // realigned paths are in the LDG form only) is split in two when its aligned
+  // segments alone make a TMA launch of at least kSplitMinChunksPerSm chunks per
+  // SM: those first, then the others on the LDG form (the units are
+  // independent, as the order above already assumes). Measured on GB300
+  // (interleaved A/B, one LDG launch -> TMA launch + LDG launch; local-rank
+  // steps of four aligned units and two with odd shard lengths): aligned
+  // segments of 5.8 GB (about 740 chunks per SM) 0.774 -> 0.865 of the copy
+  // peak, of 2.1 GB (about 270 per SM) 0.793 -> 0.870, of 0.73 GB (about 92 per
+  // SM) 0.761 -> 0.728: the second launch costs tens of microseconds.
+  int64_t aligned_chunks = 0;
+  int dev = 0, sms = 0;
+  if (!off.seg.empty()) {
+    for (const Seg& d : aligned.seg) aligned_chunks += chunks_of(d);
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      sms = 152;
+  }
+  if (!off.seg.empty() && aligned_chunks >= kSplitMinChunksPerSm * sms) {
+    int c = 0, t = 0, c_al = 0, t_al = 0, i_al = 0;
+    if (int rc = launch(ordered, s, nullptr, &c, &t, nullptr)) return rc;
+    if (int rc = launch(aligned, s, nullptr, &c_al, &t_al, &i_al)) return rc;
+    if (t < c && t_al == c_al) {
+      if (!count) {
+        if (int rc = launch(aligned, s, stream, nullptr, nullptr, nullptr)) return rc;
+        return launch(off, s, stream, nullptr, nullptr, nullptr);
+      }
+      int c_off = 0, t_off = 0, i_off = 0;
+      if (int rc = launch(off, s, nullptr, &c_off, &t_off, &i_off)) return rc;
+      *count = c_al + c_off;
+      if (tma_count) *tma_count = t_al + t_off;
+      if (interleaved_count) *interleaved_count = i_al + i_off;
+      return FSDP_OK;
     }
   }
   return launch(ordered, s, stream, count, tma_count, interleaved_count);

@@ -269,6 +269,42 @@ def test_w16_tma_form_follows_row_alignment():
     assert _plan_with_rows(16, 8, grain + 1024, S // 2 // 8 * 8) == (1, 0, 0)
 
 
+def _local_units(sizes, rank, W=8, base=BASE):
+    """Units of the local-rank step laid out as the bench lays them out (fake addresses): a
+    pool of W gradient rows as long as the largest padded unit, state and the other ranks'
+    shards as views of one buffer per quantity (rows of W x sum of S), one full buffer."""
+    lays = [fs.fsdp_flatten_layout([P], W)[0] for P in sizes]
+    S_tot, maxpad = sum(l.shard_numel for l in lays), max(l.padded_numel for l in lays)
+    region = 1 << 36
+    master, exp_avg, exp_avg_sq, others, full = (base + (i + 1) * region for i in range(5))
+    units, so, po = [], 0, 0
+    for lay in lays:
+        units.append(dict(layout=lay, grads=[base + 2 * k * maxpad for k in range(W)],
+                          master=[master + 4 * so], exp_avg=[exp_avg + 4 * so], exp_avg_sq=[exp_avg_sq + 4 * so],
+                          other_shards=[None if k == rank else others + 2 * (k * S_tot + so) for k in range(W)],
+                          full_out=[full + 2 * po]))
+        so += lay.shard_numel
+        po += lay.padded_numel
+    return units
+
+
+def test_mixed_launch_splits_off_the_segments_off_alignment():
+    """A grouped local-rank launch whose segments off 16-byte alignment (odd shard lengths) are
+    too many for the TMA form is split in two when its aligned segments alone make a TMA
+    launch of at least 256 chunks per SM (152 SMs without a GPU); otherwise it stays one
+    launch (few such segments: one TMA launch; too few aligned chunks: one LDG launch)."""
+    big, odd = [8 * 7_400_000] * 4, [8 * 3_000_001 - 3, 8 * 2_000_007 - 5]
+    assert fs.fsdp_shard_step_grouped_plan(_local_units(big + odd, 6), 6, 7) == (2, 1)
+    assert fs.fsdp_shard_step_grouped_plan(_local_units(big, 6), 6, 7) == (1, 1)
+    assert fs.fsdp_shard_step_grouped_plan(_local_units(odd, 6), 6, 7) == (1, 0)
+    # a small odd unit among the aligned ones rides in the one TMA launch
+    assert fs.fsdp_shard_step_grouped_plan(_local_units(big + [8 * 1001 - 1, 8 * 1007 - 3], 6), 6, 7) == (1, 1)
+    # aligned segments of about 90 chunks per SM: one LDG launch (the second launch would cost more)
+    small = [8 * 2_600_000] * 4
+    assert fs.fsdp_shard_step_grouped_plan(_local_units(small, 6), 6, 7) == (1, 1)
+    assert fs.fsdp_shard_step_grouped_plan(_local_units(small + odd, 6), 6, 7) == (1, 0)
+
+
 def test_pack_unpack_reject_bad_arguments():
     lay, offs = fs.fsdp_flatten_layout([10, 20, 30], 4)
     ts = [_addr(k) for k in range(3)]

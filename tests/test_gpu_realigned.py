@@ -12,8 +12,9 @@ instead of falling back to one element per thread. Cases: all ranks at W = 2,
 (R, padded) buffer per quantity), hybrid groups, the local-rank mode over units
 of odd sizes, special values with every state phase (0, 4, 8, 12 bytes), and
 the one-launch reduce-scatter and grouped Adam on arrays at their own phases,
-and copies (pack, unpack, all-gather) whose sources and destinations start at
-their own byte phases.
+copies (pack, unpack, all-gather) whose sources and destinations start at
+their own byte phases, and a grouped launch split into a TMA launch of its
+aligned segments and an LDG launch of the others.
 """
 import numpy as np
 import pytest
@@ -228,3 +229,28 @@ def test_realigned_copies(ora, seed):
     fs.fsdp_all_gather(sd, glay, full)
     gu.assert_same_bits(gu.to_host(full), ora.all_gather(shards), "all-gather")
     assert _canaries(gbuf, go, W * S, 11), "write outside the full buffer"
+
+
+def test_mixed_launch_split(ora):
+    """A local-rank launch of four aligned units and two with odd shard lengths (their sum a
+    multiple of 8, so that the other ranks' shards, rows of one (W, sum of S) buffer, stay
+    aligned for the aligned units), large enough that the aligned segments alone make a
+    TMA launch of at least 256 chunks per SM while the whole holds too many segments off
+    alignment for it: the library splits it into a TMA launch of the aligned segments and
+    an LDG launch of the others. Every element of every unit."""
+    torch = gu.torch()
+    W, rank = 8, 6
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    S_al = 7_400_000 * max(1, -(-sms // 152))
+    sizes = [8 * S_al] * 4 + [8 * 3_000_001 - 3, 8 * 2_000_007 - 5]
+    wl = wls.Workload("mixed_local", 11, [[(P,)] for P in sizes], W, sigma_state=1e-4)
+    units, info, bufs = bench.build_local_rank(wl, rank, torch, fs, synth)
+    assert [u["layout"].shard_numel % 2 for u in units] == [0] * 4 + [1, 1]
+    assert fs.fsdp_shard_step_grouped_plan(units, rank, rank + 1) == (2, 1)
+    assert fs.fsdp_shard_step_grouped_plan(units[4:], rank, rank + 1) == (1, 0)
+    fs.fsdp_device_status(clear=True)
+    fs.fsdp_shard_step_grouped(units, rank, rank + 1, gu.adam_hyper(5))
+    torch.cuda.synchronize()
+    assert fs.fsdp_device_status() == 0
+    _every_element(ora, wl, units, rank, rank + 1, 5, "mixed local")
+    del units, bufs

@@ -61,6 +61,14 @@ def _draw_units(rng, local, need_chunks):
         units.append([(P,)])
     for _ in range(int(rng.integers(1, 4))):
         units.append([(int(rng.integers(1, 6000)) | 1,)])
+    if local:
+        # one more tiny unit, so that the odd units' shard lengths sum to a multiple of 8:
+        # the other ranks' shards are rows of one (W, sum of S) buffer, which stay 16-byte
+        # aligned for the aligned units (else every gather lies off alignment, and the
+        # launch takes the LDG form)
+        odd = sum(-(-u[0][0] // W) for u in units if u[0][0] % (8 * W))
+        if odd % 8:
+            units.append([(W * (8 - odd % 8) - 1,)])
     return units
 
 
