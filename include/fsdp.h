@@ -262,7 +262,10 @@ typedef struct {
  * when they fit the launch's descriptor table, else in as few as needed.
  * The launch runs every unit's fused step first and then every unit's gather
  * of the other ranks' shards (the two touch disjoint memory, so the order
- * does not change any result). All units share W, F, the owned rank range
+ * does not change any result). When many of the segments lie off 16-byte
+ * alignment (shard lengths not a multiple of 8) and the aligned ones alone
+ * fill the TMA form, the aligned segments go in a first launch and the
+ * others in a second (again no result changes). All units share W, F, the owned rank range
  * and the hyper-parameters. Units must not share output memory.
  * n_units == 0 is a no-op. */
 int fsdp_shard_step_grouped(const fsdp_unit_args_t *units, int32_t n_units, int32_t rank_begin,
@@ -280,7 +283,8 @@ int fsdp_shard_step_grouped_launches(const fsdp_unit_args_t *units, int32_t n_un
  * copies into a shared-memory pipeline; chosen for W = 8 launches made of
  * one-replica step segments, and copies, for W = 16 ones whose gradient rows
  * do not all lie a multiple of 2 KB apart, and for launches of copies only, each with
- * enough chunks to fill every SM's pipeline), *tma_interleaved_out (if not
+ * enough chunks to fill every SM's pipeline and at most one eighth of its step
+ * and of its copy chunks off 16-byte alignment), *tma_interleaved_out (if not
  * NULL) how many of the W = 8 TMA launches stage their step chunks in four
  * interleaved rounds of quarter-chunk copies (chosen when a launch's gradient
  * rows span 3 GiB or more of addresses).
