@@ -232,6 +232,25 @@ __device__ __forceinline__ void add_row(float (&acc)[8], const RowLoad<kSplit>& 
   }
 }
 
+// A request that the line holding x be brought into L2; it returns no data
+// and holds no register.
+__device__ __forceinline__ void prefetch_l2(const void* x) {
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(x));
+}
+
+// The lines of the thread's 8 elements (from e) in its block's next chunk of
+// the same segment, for every gradient row and the first replica's three state
+// arrays: requested into L2 now, read one round of the grid later (the block's
+// next chunk is gridDim.x chunks on). Only elements inside the segment.
+template <int W>
+__device__ __forceinline__ void prefetch_next_step(const Params& p, const Seg& d, int64_t e) {
+  const int64_t en = e + int64_t(gridDim.x) * kChunkElems;
+  if (en + kVec > d.n) return;
+  const int w = W > 0 ? W : p.s.w;
+  for (int k = 0; k < w; ++k) prefetch_l2(static_cast<const uint16_t*>(p.ptr[d.ptr + k]) + en);
+  for (int a = 0; a < 3; ++a) prefetch_l2(static_cast<const float*>(p.ptr[d.ptr + w + a]) + en);
+}
+
 // The 16 bytes that start `phase` bytes (0..15) into the aligned block lo, hi
 // being the aligned block after it: a shift by whole words (phase / 4, by
 // selects on its two bits: the phase is the same for every thread of a row or
@@ -474,6 +493,12 @@ __device__ __noinline__ void step_chunk_realigned(const Params& p, const Seg& d,
     return;
   }
   const int64_t e = ew + int64_t(lane) * kVec;
+  // at W = 2 and 4 the next chunk's lines are requested into L2 first.
+  // Measured on GB300 (interleaved A/B, odd S, about 1e8 elements, all ranks):
+  // W = 2 0.620 -> 0.713 of the copy peak, W = 4 0.637 -> 0.652; W = 8 and 16
+  // lost 2-9 % with it (their loads already fill the memory pipeline), and so
+  // did every aligned LDG step (7-15 %).
+  if constexpr (W == 2 || W == 4) prefetch_next_step<W>(p, d, e);
   const int b0 = d.ptr + w;
   State8 st;
   load_f32x8_any(static_cast<const float*>(p.ptr[b0]) + e, st.p);
