@@ -70,6 +70,25 @@ def test_odd_shards_all_ranks(ora, W, F):
     del units, keep
 
 
+@pytest.mark.parametrize("W", [2, 4])
+def test_odd_shards_with_next_chunk_prefetch(ora, W):
+    """At W = 2 and 4 the realigned step requests its block's next chunk into L2 before its
+    loads; shards of about 1e6 elements give every block a next chunk in the same segment
+    (the grid holds 3 blocks per SM), so the requests are issued. Every element."""
+    torch = gu.torch()
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    S = 2048 * 3 * sms * 2 + 1  # two rounds of the grid per rank, odd
+    n = W * S - 1
+    wl = bench.sweep_workload(n, W)
+    units, info, keep = bench.build_all_ranks(wl, W, torch, fs, synth)
+    assert units[0]["layout"].shard_numel == S
+    assert fs.fsdp_shard_step_grouped_plan(units, 0, W) == (1, 0)
+    fs.fsdp_shard_step_grouped(units, 0, W, gu.adam_hyper(6))
+    torch.cuda.synchronize()
+    _every_element(ora, wl, units, 0, W, 6, "odd S with prefetch, W=%d" % W)
+    del units, keep
+
+
 def test_odd_units_local_rank(ora):
     """The local-rank mode over units of odd sizes: each unit's rows, gathered slices and
     state views (one buffer per quantity) start at their own phases."""
@@ -152,7 +171,7 @@ def test_realigned_adam_grouped(ora, offs):
     specials = np.array([np.inf, -np.inf, np.nan, 0.0, -0.0, 1e-40, -1e-40, 3.3e38, -3.3e38, 1e-3],
                         dtype=np.float32)
     shards, want = [], []
-    for n in (100_003, 65_536 + 5):
+    for n in (100_003, 65_536 + 5, 2_000_003):  # the last gives blocks a next chunk (prefetched)
         g = (rng.standard_normal(n) * 1e-2).astype(np.float32)
         idx = rng.choice(n, size=n // 16, replace=False)
         g[idx] = rng.choice(specials, size=idx.size)
