@@ -566,13 +566,20 @@ int grouped(const fsdp_unit_args_t* units, int32_t n_units, int32_t rank_begin, 
   // 8.562 -> 8.471 ms (two boxes), four Llama blocks 1.031 -> 1.006 ms, GPT-2
   // small 0.173 -> 0.165 ms; the gathers first instead were 2 % slower than this
   // on the last two and equal on the 7B step.
+  // (the aligned and off-alignment lists below are built only when some
+  // segment is off alignment: the common launch pays for one list)
+  auto off_alignment = [](const Seg& d) { return d.kind == kCopy ? d.width != 16 : d.width == kPhased; };
+  bool any_off = false;
+  for (const Seg& d : list.seg) any_off = any_off || off_alignment(d);
   SegmentList ordered, aligned, off;
+  ordered.seg.reserve(list.seg.size());
+  ordered.ptr.reserve(list.ptr.size());
   for (int pass = 0; pass < 2; ++pass) {
     for (size_t i = 0; i < list.seg.size(); ++i) {
       const Seg& d = list.seg[i];
       if ((pass == 0) != (d.kind == kStep)) continue;
-      const bool phased = d.kind == kCopy ? d.width != 16 : d.width == kPhased;
-      for (SegmentList* to : {&ordered, phased ? &off : &aligned}) {
+      for (SegmentList* to : {&ordered, any_off ? (off_alignment(d) ? &off : &aligned) : nullptr}) {
+        if (!to) continue;
         Seg e = d;
         e.ptr = static_cast<int32_t>(to->ptr.size());
         to->seg.push_back(e);
