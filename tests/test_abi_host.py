@@ -305,6 +305,37 @@ def test_mixed_launch_splits_off_the_segments_off_alignment():
     assert fs.fsdp_shard_step_grouped_plan(_local_units(small + odd, 6), 6, 7) == (1, 0)
 
 
+def _all_ranks_units(sizes, W=8, base=BASE):
+    """All-ranks units laid out as the bench lays them out (fake addresses): per unit a
+    (W, padded) gradient buffer, one (W, S) buffer per state quantity, one full buffer."""
+    units, addr = [], base
+    for P in sizes:
+        lay = fs.fsdp_flatten_layout([P], W)[0]
+        S, padded = lay.shard_numel, lay.padded_numel
+        grads = [addr + 2 * k * padded for k in range(W)]
+        addr += -(-2 * W * padded // 4096) * 4096
+        state = []
+        for _ in range(3):
+            state.append([addr + 4 * r * S for r in range(W)])
+            addr += -(-4 * W * S // 4096) * 4096
+        units.append(dict(layout=lay, grads=grads, master=state[0], exp_avg=state[1], exp_avg_sq=state[2],
+                          other_shards=None, full_out=[addr]))
+        addr += -(-2 * padded // 4096) * 4096
+    return units
+
+
+def test_mixed_all_ranks_launch_splits_too():
+    """The same split for the all-ranks step: a unit with an odd shard length has every rank's
+    slice but rank 0's off alignment; beside three large aligned units it sends the whole
+    launch to the LDG form, so the aligned segments (rank 0's slice included) go first on
+    the TMA form."""
+    big, odd = [8 * 4_000_000] * 3, [8 * 4_000_001 - 1]
+    assert fs.fsdp_shard_step_grouped_plan(_all_ranks_units(big + odd), 0, 8) == (2, 1)
+    assert fs.fsdp_shard_step_grouped_plan(_all_ranks_units(big), 0, 8) == (1, 1)
+    assert fs.fsdp_shard_step_grouped_plan(_all_ranks_units(odd), 0, 8) == (1, 0)
+    assert fs.fsdp_shard_step_grouped_plan(_all_ranks_units(big[:1] + odd), 0, 8) == (1, 0)
+
+
 def test_pack_unpack_reject_bad_arguments():
     lay, offs = fs.fsdp_flatten_layout([10, 20, 30], 4)
     ts = [_addr(k) for k in range(3)]
