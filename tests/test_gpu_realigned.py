@@ -13,8 +13,8 @@ instead of falling back to one element per thread. Cases: all ranks at W = 2,
 of odd sizes, special values with every state phase (0, 4, 8, 12 bytes), and
 the one-launch reduce-scatter and grouped Adam on arrays at their own phases,
 copies (pack, unpack, all-gather) whose sources and destinations start at
-their own byte phases, and a grouped launch split into a TMA launch of its
-aligned segments and an LDG launch of the others.
+their own byte phases, and grouped launches (local-rank and all-ranks) split
+into a TMA launch of their aligned segments and an LDG launch of the others.
 """
 import numpy as np
 import pytest
@@ -273,3 +273,25 @@ def test_mixed_launch_split(ora):
     assert fs.fsdp_device_status() == 0
     _every_element(ora, wl, units, rank, rank + 1, 5, "mixed local")
     del units, bufs
+
+
+def test_mixed_all_ranks_launch_split(ora):
+    """The all-ranks step of three aligned units and one with an odd shard length (every
+    rank's slice but rank 0's off alignment): split into a TMA launch of the aligned
+    segments (rank 0's slice of the odd unit included) and an LDG launch of the others.
+    Every element of every rank of every unit."""
+    torch = gu.torch()
+    W = 8
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    S_al = 4_000_000 * max(1, -(-sms // 152))
+    sizes = [8 * S_al] * 3 + [8 * 4_000_001 - 1]
+    wl = wls.Workload("mixed_all_ranks", 13, [[(P,)] for P in sizes], W, sigma_state=1e-4)
+    units, info, keep = bench.build_all_ranks(wl, W, torch, fs, synth)
+    assert units[-1]["layout"].shard_numel % 2 == 1
+    assert fs.fsdp_shard_step_grouped_plan(units, 0, W) == (2, 1)
+    fs.fsdp_device_status(clear=True)
+    fs.fsdp_shard_step_grouped(units, 0, W, gu.adam_hyper(8))
+    torch.cuda.synchronize()
+    assert fs.fsdp_device_status() == 0
+    _every_element(ora, wl, units, 0, W, 8, "mixed all ranks")
+    del units, keep
